@@ -1,0 +1,210 @@
+"""Pins for the fp64 oracle, against facts that do not come from the oracle.
+
+Each test is chosen so that a plausible slip in oracle.c -- a transposed
+operand, a swapped index, a dropped or doubled term, a wrong sign, a wrong
+widening of a format -- fails at least one of them:
+
+  * hand-worked products (tests/golden/hand_products.txt), non-square, signed;
+  * identity and permutation matrices (exact);
+  * rank-1 closed forms and all-ones inputs (exact on small integers);
+  * the sum identity sum_ij C_ij = sum_k colsum(A)_k rowsum(B)_k;
+  * S == C on non-negative inputs, S invariant under sign flips;
+  * known bit patterns of the BF16 and TF32 formats;
+  * agreement with numpy's float64 matmul (a library routine) on small inputs,
+    within the float64 summation bound.
+CPU only.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from accelerator_gb300 import inputs
+from golden_io import hand_products
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+@pytest.mark.parametrize("case", hand_products(), ids=lambda c: c["name"])
+def test_hand_worked_products(case):
+    C, S = oracle.gemm(case["A"], case["B"], fmt="f64")
+    np.testing.assert_array_equal(C, case["C"])
+    if "S" in case:
+        np.testing.assert_array_equal(S, case["S"])
+    # the same values given as float32 (all are exact in binary32)
+    C32, _ = oracle.gemm(_f32(case["A"]), _f32(case["B"]), fmt="f32")
+    np.testing.assert_array_equal(C32, case["C"])
+
+
+@pytest.mark.parametrize("M,K,N", [(5, 7, 3), (1, 9, 4), (6, 1, 6)])
+def test_identity(M, K, N):
+    A, B = inputs.matrices(M, K, N, "pm1", seed=3)
+    C, _ = oracle.gemm(A, np.eye(K, dtype=np.float32))
+    np.testing.assert_array_equal(C, A.astype(np.float64))      # A * I = A
+    C, _ = oracle.gemm(np.eye(K, dtype=np.float32), B)
+    np.testing.assert_array_equal(C, B.astype(np.float64))      # I * B = B
+
+
+def test_permutation():
+    rng = np.random.default_rng(7)
+    M, K, N = 6, 5, 8
+    A, B = inputs.matrices(M, K, N, "pm1", seed=4)
+    pi = rng.permutation(K)
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), pi] = 1.0           # (A P)[:, pi[k]] = A[:, k]
+    C, _ = oracle.gemm(A, P)
+    expect = np.empty((M, K))
+    expect[:, pi] = A
+    np.testing.assert_array_equal(C, expect)
+    Q = np.zeros((K, K), np.float32)
+    Q[np.arange(K), pi] = 1.0           # (Q B)[k, :] = B[pi[k], :]
+    C, _ = oracle.gemm(Q, B)
+    np.testing.assert_array_equal(C, B[pi].astype(np.float64))
+
+
+def test_rank_one_closed_forms():
+    rng = np.random.default_rng(11)
+    M, K, N = 7, 13, 5
+    u = rng.integers(-5, 6, M).astype(np.float32)
+    v = rng.integers(-5, 6, N).astype(np.float32)
+    # A = u 1^T, B = 1 v^T  ->  C_ij = K u_i v_j
+    A = np.repeat(u[:, None], K, axis=1)
+    B = np.repeat(v[None, :], K, axis=0)
+    C, _ = oracle.gemm(A, B)
+    np.testing.assert_array_equal(C, K * np.outer(u, v).astype(np.float64))
+    # A = u a^T, B = b v^T  ->  C = (a . b) u v^T
+    a = rng.integers(-3, 4, K).astype(np.float32)
+    b = rng.integers(-3, 4, K).astype(np.float32)
+    C, _ = oracle.gemm(np.outer(u, a).astype(np.float32), np.outer(b, v).astype(np.float32))
+    ab = float(sum(int(x) * int(y) for x, y in zip(a, b)))
+    np.testing.assert_array_equal(C, ab * np.outer(u, v).astype(np.float64))
+
+
+@pytest.mark.parametrize("K", [0, 1, 2, 777])
+def test_all_ones(K):
+    C, S = oracle.gemm(np.ones((3, K), np.float32), np.ones((K, 4), np.float32))
+    np.testing.assert_array_equal(C, np.full((3, 4), float(K)))
+    np.testing.assert_array_equal(S, np.full((3, 4), float(K)))
+
+
+def test_empty_dims():
+    C, S = oracle.gemm(np.ones((0, 3), np.float32), np.ones((3, 4), np.float32))
+    assert C.shape == (0, 4) and S.shape == (0, 4)
+    C, S = oracle.gemm(np.ones((2, 3), np.float32), np.ones((3, 0), np.float32))
+    assert C.shape == (2, 0)
+    C, S = oracle.gemm(np.ones((2, 0), np.float32), np.ones((0, 3), np.float32))
+    np.testing.assert_array_equal(C, np.zeros((2, 3)))          # the empty sum
+    assert oracle.total(np.ones((2, 0), np.float32), np.ones((0, 3), np.float32)) == (0.0, 0.0)
+
+
+def test_sum_identity_integers():
+    A, B = inputs.matrices(37, 29, 41, "int4", seed=5)
+    C, S = oracle.gemm(A, B)
+    t, ta = oracle.total(A, B)
+    # every partial sum here is an integer below 2**53: both sides are exact
+    assert t == float(np.sum(C)) and ta == float(np.sum(S))
+    assert t == float(np.sum(A.astype(np.int64) @ B.astype(np.int64)))
+
+
+@pytest.mark.parametrize("fmt", ["f32", "bf16", "tf32"])
+def test_sum_identity_random(fmt):
+    A, B = inputs.matrices(33, 65, 47, "pm1", seed=6)
+    if fmt == "bf16":
+        A, B = inputs.bf16_bits(A), inputs.bf16_bits(B)
+    C, S = oracle.gemm(A, B, fmt=fmt)
+    t, ta = oracle.total(A, B, fmt=fmt)
+    assert math.isclose(t, math.fsum(C.ravel()), rel_tol=1e-12, abs_tol=1e-12 * ta)
+    assert math.isclose(ta, math.fsum(S.ravel()), rel_tol=1e-12)
+
+
+def test_scale_against_value():
+    A, B = inputs.matrices(19, 23, 17, "u01", seed=8)
+    C, S = oracle.gemm(A, B)
+    np.testing.assert_array_equal(S, C)                  # all terms >= 0
+    A2, B2 = inputs.matrices(19, 23, 17, "pm1", seed=8)
+    C2, S2 = oracle.gemm(A2, B2)
+    assert np.all(S2 >= np.abs(C2))
+    Cn, Sn = oracle.gemm(-A2, B2)
+    np.testing.assert_array_equal(Cn, -C2)
+    np.testing.assert_array_equal(Sn, S2)
+    Ca, _ = oracle.gemm(np.abs(A2), np.abs(B2))
+    np.testing.assert_array_equal(Ca, S2)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 1), (16, 64, 16), (33, 17, 64), (64, 64, 64)])
+@pytest.mark.parametrize("dist", ["u01", "pm1"])
+def test_against_numpy_float64(M, K, N, dist):
+    A, B = inputs.matrices(M, K, N, dist, seed=M * 1000 + N)
+    C, S = oracle.gemm(A, B)
+    ref = A.astype(np.float64) @ B.astype(np.float64)
+    # two float64 sums of the same K exact products differ by at most
+    # 2 * gamma_K * S with gamma_K = K u / (1 - K u), u = 2**-53
+    g = K * 2.0 ** -53 / (1 - K * 2.0 ** -53)
+    assert np.all(np.abs(C - ref) <= 2 * g * S + 1e-300)
+
+
+def test_dot_matches_full():
+    A, B = inputs.matrices(40, 50, 60, "pm1", seed=9)
+    C, S = oracle.gemm(A, B)
+    rows, cols = inputs.sample_indices(40, 60, n=300, seed=9)
+    c, s = oracle.dot(A, B, rows, cols)
+    np.testing.assert_array_equal(c, C[rows, cols])     # same k order: bit-identical
+    np.testing.assert_array_equal(s, S[rows, cols])
+
+
+def test_dot_rejects_bad_index():
+    A, B = inputs.matrices(4, 5, 6, "u01")
+    with pytest.raises(RuntimeError):
+        oracle.dot(A, B, [4], [0])
+    with pytest.raises(RuntimeError):
+        oracle.dot(A, B, [0], [-1])
+
+
+def test_thread_count_does_not_change_results():
+    A, B = inputs.matrices(31, 200, 29, "pm1", seed=10)
+    C1, S1 = oracle.gemm(A, B, nthreads=1)
+    C4, S4 = oracle.gemm(A, B, nthreads=4)
+    np.testing.assert_array_equal(C1, C4)
+    np.testing.assert_array_equal(S1, S4)
+
+
+def test_bf16_widening_known_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0000, 0x8000, 0x7F7F, 0x0001, 0x4049],
+                    np.uint16)
+    want = [1.0, -2.0, 1.0 + 2.0 ** -7, 0.0, -0.0, (2 - 2.0 ** -7) * 2.0 ** 127,
+            2.0 ** -133, 3.140625]
+    got = oracle.widen(bits, "bf16")
+    assert list(got) == want
+
+
+def test_tf32_truncation_known_values():
+    x = np.array([1.0, 1.0 + 2.0 ** -10, 1.0 + 2.0 ** -11, 1.0 + 2.0 ** -23,
+                  -(1.0 + 2.0 ** -10 + 2.0 ** -11), 3.0, 2.0 ** -126 * (1 + 2.0 ** -12)],
+                 np.float32)
+    want = [1.0, 1.0 + 2.0 ** -10, 1.0, 1.0, -(1.0 + 2.0 ** -10), 3.0, 2.0 ** -126]
+    assert list(oracle.widen(x, "tf32")) == want
+    # f32 format widens unchanged
+    assert list(oracle.widen(x, "f32")) == [float(v) for v in x]
+
+
+def test_formats_agree_on_exact_inputs():
+    # integers -4..4 are exact in every format, so every format gives one C
+    A, B = inputs.matrices(9, 31, 11, "int4", seed=12)
+    ref, _ = oracle.gemm(A, B, fmt="f32")
+    for fmt, (a, b) in {"tf32": (A, B), "bf16": (inputs.bf16_bits(A), inputs.bf16_bits(B)),
+                        "f64": (A.astype(np.float64), B.astype(np.float64))}.items():
+        C, _ = oracle.gemm(a, b, fmt=fmt)
+        np.testing.assert_array_equal(C, ref)
+
+
+def test_rejects_bad_arguments():
+    A = np.ones((2, 3), np.float32)
+    with pytest.raises(ValueError):
+        oracle.gemm(A, np.ones((4, 2), np.float32))
+    with pytest.raises(TypeError):
+        oracle.gemm(A, np.ones((3, 2), np.float64))
+    with pytest.raises(ValueError):
+        oracle.gemm(A, np.ones((3, 2), np.float32), fmt="fp8")
