@@ -1,0 +1,257 @@
+// api.cu -- the C ABI of libgemm (include/gemm.h): argument checks, the
+// choice of kernel, TMA descriptors, scratch for re-strided operands, and the
+// device error word.  Host code only, apart from the error word itself.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace libgemm;
+
+// One per device (a __device__ variable exists once per device context).
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single pipeline wait
+
+struct DeviceState {
+    bool ready = false;
+    int status = GEMM_OK;
+    int num_sms = 0;
+    unsigned* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int64_t> g_launches{0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up, once: device check, SM count, error word address,
+// kernel attributes, and the driver's tensor-map encoder.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        st.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_error_word) != cudaSuccess ||
+                   ffma_setup() != cudaSuccess || tc_setup() != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                st.status = GEMM_ERR_CUDA;
+            else
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        if (st.status != GEMM_OK) cudaGetLastError();   // do not leave a stale error behind
+    }
+    *out = &st;
+    return st.status;
+}
+
+bool ranges_overlap(uintptr_t a, uint64_t abytes, uintptr_t b, uint64_t bbytes) {
+    if (abytes == 0 || bbytes == 0) return false;
+    return a < b + bbytes && b < a + abytes;
+}
+
+// 2-D tensor map over a rows x cols row-major matrix with row stride ld
+// (elements), box box_cols x box_rows, 128-byte swizzle, zero fill outside.
+int encode_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols, int64_t ld,
+              int box_cols, int box_rows) {
+    const CUtensorMapDataType dt =
+        es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
+                     int64_t N, DeviceState* st, cudaStream_t stream) {
+    const int es = mode == TcMode::kBF16 ? 2 : 4;
+    const TcShape shape = tc_shape(mode);
+    const int64_t align_elems = 16 / es;
+    // BF16 reads B as an MN-major operand, straight from the caller's K x N
+    // rows.  The MN-major form of kind::tf32 returned zeros on GB300, so the
+    // TF32 kernel reads B^T (N x K, K-major), made by a transpose pass.
+    const bool b_k_major = mode == TcMode::kTF32;
+    // TMA wants 16-byte aligned bases and row strides that are multiples of 16 bytes.
+    const bool pad_a = (K % align_elems) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
+    const bool pad_b = !b_k_major &&
+                       ((N % align_elems) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0);
+    const int64_t lda = pad_a ? round_up(K, align_elems) : K;
+    const int64_t ldb = b_k_major ? round_up(K, align_elems) : (pad_b ? round_up(N, align_elems) : N);
+    const int64_t a_bytes = pad_a ? round_up(M * lda * es, 256) : 0;
+    const int64_t b_bytes = b_k_major ? round_up(N * ldb * es, 256) : (pad_b ? round_up(K * ldb * es, 256) : 0);
+
+    void* scratch = nullptr;
+    const void* a_use = A;
+    const void* b_use = B;
+    if (a_bytes + b_bytes > 0) {
+        if (cudaMallocAsync(&scratch, (size_t)(a_bytes + b_bytes), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NO_MEMORY;
+        }
+        uint8_t* s = static_cast<uint8_t*>(scratch);
+        int rc = GEMM_OK;
+        if (pad_a) {
+            if (launch_restride(A, s, M, K, K, lda, es, stream) != cudaSuccess) rc = GEMM_ERR_CUDA;
+            g_launches++;
+            a_use = s;
+        }
+        if (rc == GEMM_OK && b_bytes > 0) {
+            cudaError_t e = b_k_major ? launch_transpose(B, s + a_bytes, K, N, ldb, es, stream)
+                                      : launch_restride(B, s + a_bytes, K, N, N, ldb, es, stream);
+            if (e != cudaSuccess) rc = GEMM_ERR_CUDA;
+            g_launches++;
+            b_use = s + a_bytes;
+        }
+        if (rc != GEMM_OK) {
+            cudaFreeAsync(scratch, stream);
+            return rc;
+        }
+    }
+
+    CUtensorMap map_a, map_b;
+    int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m);
+    if (rc == GEMM_OK)
+        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, shape.block_n)
+                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems);
+    if (rc == GEMM_OK) {
+        const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+        if (launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
+                           st->num_sms, st->err, kWaitLimitNs, stream) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        else
+            g_launches++;
+    }
+    if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
+    return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
+         int precision_mode, struct CUstream_st* stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16)
+        return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || K < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
+    // Every dimension must fit the kernels' 32-bit indices and TMA coordinates.
+    const int64_t kDimMax = 0x7FFFFFFF;
+    if (M > kDimMax || K > kDimMax || N > kDimMax) return GEMM_ERR_INVALID_ARG;
+    const int es = precision_mode == GEMM_BF16 ? 2 : 4;
+    const int64_t kElemMax = INT64_MAX / 16;
+    if ((K && M > kElemMax / K) || (N && K > kElemMax / N) || (N && M > kElemMax / N))
+        return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 3u) || (reinterpret_cast<uintptr_t>(A) & (es - 1)) ||
+        (reinterpret_cast<uintptr_t>(B) & (es - 1)))
+        return GEMM_ERR_MISALIGNED;
+    const uint64_t c_bytes = (uint64_t)(M * N) * 4;
+    if (K > 0 && (ranges_overlap((uintptr_t)C, c_bytes, (uintptr_t)A, (uint64_t)(M * K) * es) ||
+                  ranges_overlap((uintptr_t)C, c_bytes, (uintptr_t)B, (uint64_t)(K * N) * es)))
+        return GEMM_ERR_INVALID_ARG;
+
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != GEMM_OK) return rc;
+
+    if (K == 0) {
+        if (launch_fill_zero(C, M * N, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        g_launches++;
+        return GEMM_OK;
+    }
+    if (precision_mode == GEMM_FP32) {
+        const bool b_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+        const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+        if (launch_ffma_sgemm(static_cast<const float*>(A), static_cast<const float*>(B), C, (int)M,
+                              (int)N, (int)K, b_vec, c_vec, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_launches++;
+        return GEMM_OK;
+    }
+    return tensor_core_gemm(precision_mode == GEMM_BF16 ? TcMode::kBF16 : TcMode::kTF32, A, B, C,
+                            M, K, N, st, stream);
+}
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case GEMM_ERR_CUDA: return "CUDA error";
+    case GEMM_ERR_NO_MEMORY: return "scratch allocation failed";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    default: return "unknown status";
+    }
+}
+
+int gemm_debug_status(struct CUstream_st* stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != GEMM_OK) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, st->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (word == 0) return GEMM_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpy(st->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_ERR_TIMEOUT;
+}
+
+int gemm_version(void) { return 100; }
+
+int64_t gemm_launch_count(void) { return g_launches.load(); }
+
+int gemm_selftest_bounded_wait(int64_t timeout_ns, struct CUstream_st* stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != GEMM_OK) return rc;
+    if (timeout_ns < 1000) timeout_ns = 1000;
+    if (timeout_ns > 2000000000) timeout_ns = 2000000000;
+    rc = gemm_debug_status(stream_);   // start from a clear error word
+    if (rc != GEMM_OK && rc != GEMM_ERR_TIMEOUT) return rc;
+    if (launch_wait_selftest(st->err, (uint64_t)timeout_ns, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    g_launches++;
+    return gemm_debug_status(stream_);
+}
+
+}  // extern "C"

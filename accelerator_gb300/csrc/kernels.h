@@ -1,0 +1,43 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels.  Not installed; callers use include/gemm.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace libgemm {
+
+// ---- exact-FP32 CUDA-core GEMM (ffma_sgemm.cu) ----
+// b_vec: B rows may be copied 16 bytes at a time (N % 4 == 0, B 16-byte aligned).
+// c_vec: C rows may be stored 16 bytes at a time (N % 4 == 0, C 16-byte aligned).
+cudaError_t ffma_setup();
+cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
+                              bool b_vec, bool c_vec, cudaStream_t stream);
+
+// ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
+enum class TcMode { kBF16, kTF32 };
+struct TcShape {
+    int block_m, block_n;   // output tile per CTA
+    int k_elems;            // K elements per pipeline stage (128 bytes)
+    int b_box_n;            // N extent of one TMA box of B (128 bytes)
+};
+TcShape tc_shape(TcMode mode);
+cudaError_t tc_setup();
+// b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
+cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+                           const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
+                           int num_sms, unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+
+// ---- helpers (prep.cu) ----
+// Copy a rows x cols matrix of es-byte elements from row stride src_ld to
+// row stride dst_ld (both in elements).
+cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t cols,
+                            int64_t src_ld, int64_t dst_ld, int es, cudaStream_t stream);
+// dst (cols x rows, row stride dst_ld elements) = transpose of src (rows x cols, dense).
+cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
+                             int64_t dst_ld, int es, cudaStream_t stream);
+cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace libgemm

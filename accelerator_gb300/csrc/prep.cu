@@ -1,0 +1,122 @@
+// prep.cu -- small helper kernels of libgemm.
+//
+//   restride    copies an operand into a buffer whose row stride is a multiple
+//               of 16 bytes, for the tensor-core path when TMA cannot describe
+//               the caller's layout (e.g. K = 777 floats: 3108-byte rows).
+//   fill_zero   C := 0 for K == 0 (the empty sum).
+//   wait_selftest  one CTA waits on an mbarrier that nothing completes, to
+//               show the bounded wait gives up and reports instead of hanging.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace libgemm {
+namespace {
+
+template <typename T>
+__global__ void restride_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
+                                int64_t cols, int64_t src_ld, int64_t dst_ld) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const T* s = src + r * src_ld;
+        T* d = dst + r * dst_ld;
+        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x)
+            d[c] = s[c];
+    }
+}
+
+// 32 x 32 tiles through shared memory (one padding column keeps the
+// column-wise reads free of bank conflicts), so reads and writes are both
+// coalesced along rows.
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
+                                 int64_t cols, int64_t dst_ld) {
+    __shared__ T tile[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;   // block 32 x 8
+    const int64_t c0 = (int64_t)blockIdx.x * 32;
+    for (int64_t r0 = (int64_t)blockIdx.y * 32; r0 < rows; r0 += (int64_t)gridDim.y * 32) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            const int64_t r = r0 + ty + j, c = c0 + tx;
+            if (r < rows && c < cols) tile[ty + j][tx] = src[r * cols + c];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            const int64_t c = c0 + ty + j, r = r0 + tx;   // dst row c, column r
+            if (r < rows && c < cols) dst[c * dst_ld + r] = tile[tx][ty + j];
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        C[i] = 0.0f;
+}
+
+__global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // No thread and no copy ever arrives: phase 0 never completes.
+        (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t cols,
+                            int64_t src_ld, int64_t dst_ld, int es, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t bx = (cols + threads - 1) / threads;
+    dim3 grid((unsigned)(bx < 64 ? bx : 64), (unsigned)(rows < 65535 ? rows : 65535));
+    if (es == 4)
+        restride_kernel<uint32_t><<<grid, threads, 0, stream>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, src_ld, dst_ld);
+    else if (es == 2)
+        restride_kernel<uint16_t><<<grid, threads, 0, stream>>>(
+            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, src_ld, dst_ld);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
+                             int64_t dst_ld, int es, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
+    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535)), block(32, 8);
+    if (es == 4)
+        transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, dst_ld);
+    else if (es == 2)
+        transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(
+            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, dst_ld);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    fill_zero_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(C, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace libgemm

@@ -1,0 +1,323 @@
+// tc_gemm.cu -- tensor-core GEMM on sm_103a (modes GEMM_TF32 and GEMM_BF16).
+//
+// C_ij = sum_k A_ik B_kj ("Shared Memory Tiling for Matrix Multiplication",
+// opening formula), A M x K row-major (K-major), B K x N row-major (N-major),
+// C M x N row-major fp32.  The pages stop at naming tensor cores as the next
+// step ("Matrix Multiplication -- Naive to Tiled", section 07, "Tensor Cores");
+// this is that step written for the 5th-generation tensor cores.
+//
+// One persistent CTA per SM walks output tiles of 128 x 256.  Its six warps
+// have fixed roles:
+//   warp 0  TMA producer: one thread streams 128-byte-wide K slabs of A
+//           (128 rows) and B (256 columns) into a 4-stage shared-memory ring
+//           with cp.async.bulk.tensor; each slot has a "full" mbarrier that
+//           the copy completes and an "empty" one the MMA frees.
+//   warp 1  owns tensor memory (512 columns = two 128 x 256 fp32
+//           accumulators) and one thread issues tcgen05.mma (M=128, N=256,
+//           K=8 for TF32 / 16 for BF16), then tcgen05.commit to free the slot.
+//   warps 2-5  epilogue: tcgen05.ld the finished accumulator (each warp its
+//           32-lane quarter of TMEM), store fp32 rows of C guarded against M
+//           and N, and hand the accumulator back.  With two accumulators the
+//           epilogue of tile t overlaps the MMAs of tile t+1.
+// The ring replaces the pages' two __syncthreads per tile (first page,
+// section 05; second page's barrier discussion) by full/empty phases, and
+// the TMA's zero fill of out-of-range boxes replaces their guarded loads.
+//
+// Shared-memory operand layouts (128-byte swizzle, each tile 1024-aligned):
+//   A slab: 128 rows x 128 bytes of K, row r at r*128: the canonical K-major
+//     layout, 8-row groups 1024 bytes apart (stride byte offset 1024).  The
+//     k-th MMA of a slab starts 32*k bytes into the rows.
+//   B slab: 128/es columns of N per 128-byte row, one row per k, boxes of
+//     128/es columns side by side every (K rows * 128) bytes: the canonical
+//     MN-major layout with leading byte offset = box size, stride byte
+//     offset = 1024 (8 k-rows).  The k-th MMA starts k*UMMA_K rows down.
+//
+// Every wait is bounded (see mbar_wait): if one expires the CTA records a
+// timeout in the device error word, the roles stop, in-flight copies and
+// MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace libgemm {
+namespace {
+
+constexpr int kBM = 128, kBN = 256;
+constexpr int kStages = 4;
+constexpr int kSlabBytes = 128;                      // K bytes per stage (one swizzle row)
+constexpr int kABytes = kBM * kSlabBytes;            // 16 KB
+constexpr int kBBytes = kBN * kSlabBytes;            // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kAccCols = kBN;                        // fp32 accumulator columns per tile
+constexpr int kTmemCols = 2 * kAccCols;              // 512
+constexpr int kThreads = 192;
+constexpr int kGroupM = 8;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+template <TcMode MODE>
+struct Traits;
+template <>
+struct Traits<TcMode::kBF16> {
+    static constexpr int kEs = 2;
+    static constexpr uint32_t kFormat = 1;       // BF16
+    static constexpr TcKind kKind = TcKind::kF16;
+};
+template <>
+struct Traits<TcMode::kTF32> {
+    static constexpr int kEs = 4;
+    static constexpr uint32_t kFormat = 2;       // TF32
+    static constexpr TcKind kKind = TcKind::kTF32;
+};
+
+struct Sched {
+    int tiles_m, tiles_n;
+    __device__ __forceinline__ void coords(int tile, int& m0, int& n0) const {
+        const int per_group = kGroupM * tiles_n;
+        const int group = tile / per_group;
+        const int first_m = group * kGroupM;
+        const int gsize = min(tiles_m - first_m, kGroupM);
+        m0 = (first_m + (tile % per_group) % gsize) * kBM;
+        n0 = ((tile % per_group) / gsize) * kBN;
+    }
+};
+
+// Drain wait: bounded by time only (ignores the abort flag).
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+template <TcMode MODE, bool kBKMajor>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, float* __restrict__ C, int M, int N,
+                   int K, int tiles_m, int tiles_n, int c_vec, unsigned* err, uint64_t limit_ns) {
+    using T = Traits<MODE>;
+    constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
+    constexpr int kUmmaK = 32 / T::kEs;                   // K per MMA: 16 / 8
+    constexpr int kMmaPerStage = kKElems / kUmmaK;        // 4
+    constexpr int kBoxN = kSlabBytes / T::kEs;            // N per B box: 64 / 32
+    constexpr int kBoxes = kBN / kBoxN;                   // 4 / 8
+    constexpr uint32_t kBoxBytes = kKElems * kSlabBytes;  // 8 KB / 4 KB
+    constexpr uint32_t kIdesc = make_idesc(T::kFormat, kBM, kBN, false, !kBKMajor);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;                                   // kStages x kABytes
+    const uint32_t sB = base + kStages * kABytes;               // kStages x kBBytes
+    uint8_t* ctrl = gbase + kStages * kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
+    // bars: full[0..S), empty[S..2S), acc_full[2S..2S+2), acc_empty[2S+2..2S+4), drain[2S+4]
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStages;
+    const uint32_t accf0 = full0 + 16 * kStages, acce0 = accf0 + 16, drain_bar = acce0 + 16;
+    volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ctrl + 8 * (2 * kStages + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (2 * kStages + 5) + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 4 * 32);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_holder)), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const Sched sched{tiles_m, tiles_n};
+    const int ntiles = tiles_m * tiles_n;
+    const int nk = (K + kKElems - 1) / kKElems;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            tma_prefetch_map(&map_a);
+            tma_prefetch_map(&map_b);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t last_phase[kStages];
+            bool used[kStages];
+            for (int s = 0; s < kStages; ++s) used[s] = false, last_phase[s] = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                int m0, n0;
+                sched.coords(tile, m0, n0);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, err, limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    tma_load_2d(sA + stage * kABytes, &map_a, fb, kb * kKElems, m0);
+                    if constexpr (kBKMajor) {
+                        // B^T (N x K, K contiguous): one box of kBN rows x 128 bytes
+                        tma_load_2d(sB + stage * kBBytes, &map_b, fb, kb * kKElems, n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kBoxes; ++j)
+                            tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, &map_b, fb,
+                                        n0 + j * kBoxN, kb * kKElems);
+                    }
+                    used[stage] = true;
+                    last_phase[stage] = phase;
+                    if (++stage == kStages) stage = 0, phase ^= 1u;
+                }
+                if (!ok) break;
+            }
+            // Every copy this thread issued must have landed before the CTA exits.
+            for (int s = 0; s < kStages; ++s)
+                if (used[s] && !drain_wait(full0 + 8 * s, last_phase[s], limit_ns))
+                    atomicOr(err, kErrTimeout);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int lt = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+                const int buf = lt & 1;
+                const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait(acce0 + 8 * buf, use_parity ^ 1u, abort_flag, err, limit_ns)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kAccCols);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err, limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_tile = sA + stage * kABytes;
+                    const uint32_t b_tile = sB + stage * kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(a_tile + kk * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            kBKMajor ? smem_desc_sw128(b_tile + kk * 32, 16, 1024)
+                                     : smem_desc_sw128(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes, 1024);
+                        tc_mma<T::kKind>(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty0 + 8 * stage);   // slot is free once these MMAs are done
+                    if (++stage == kStages) stage = 0, phase ^= 1u;
+                }
+                if (!ok) break;
+                tc_commit(accf0 + 8 * buf);          // accumulator ready for the epilogue
+            }
+            // All MMAs this thread issued must be complete before TMEM is freed.
+            tc_commit(drain_bar);
+            if (!drain_wait(drain_bar, 0, limit_ns)) atomicOr(err, kErrTimeout);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+        const int row_in_tile = quarter * 32 + lane;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+            int m0, n0;
+            sched.coords(tile, m0, n0);
+            const int buf = lt & 1;
+            const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(accf0 + 8 * buf, use_parity, abort_flag, err, limit_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int row = m0 + row_in_tile;
+            float* crow = C + (int64_t)row * N;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
+#pragma unroll 1
+            for (int c = 0; c < kAccCols / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
+                tmem_ld_wait();
+                const int col0 = n0 + c * 32;
+                if (row < M) {
+                    if (c_vec && col0 + 32 <= N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(crow + col0 + j) =
+                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acce0 + 8 * buf);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+TcShape tc_shape(TcMode mode) {
+    const int es = mode == TcMode::kBF16 ? 2 : 4;
+    return TcShape{kBM, kBN, kSlabBytes / es, kSlabBytes / es};
+}
+
+template <TcMode MODE, bool BK>
+static cudaError_t set_attr() {
+    return cudaFuncSetAttribute(tc_gemm_kernel<MODE, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes);
+}
+
+cudaError_t tc_setup() {
+    cudaError_t e;
+    if ((e = set_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kBF16, true>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kTF32, false>()) != cudaSuccess) return e;
+    return set_attr<TcMode::kTF32, true>();
+}
+
+cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+                           const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
+                           int num_sms, unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
+    const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
+    const int64_t tiles = (int64_t)tiles_m * tiles_n;
+    if (tiles <= 0) return cudaSuccess;
+    if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    const int cv = c_vec ? 1 : 0;
+#define LIBGEMM_TC_LAUNCH(MODE_, BK_)                                                         \
+    tc_gemm_kernel<MODE_, BK_><<<grid, kThreads, kSmemBytes, stream>>>(                      \
+        map_a, map_b, C, M, N, K, tiles_m, tiles_n, cv, err, limit_ns)
+    if (mode == TcMode::kBF16) {
+        if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kBF16, true);
+        else LIBGEMM_TC_LAUNCH(TcMode::kBF16, false);
+    } else {
+        if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kTF32, true);
+        else LIBGEMM_TC_LAUNCH(TcMode::kTF32, false);
+    }
+#undef LIBGEMM_TC_LAUNCH
+    return cudaGetLastError();
+}
+
+}  // namespace libgemm

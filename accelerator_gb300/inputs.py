@@ -81,3 +81,10 @@ def sample_indices(M: int, N: int, n: int = 4096, seed: int = BASE_SEED):
     rows = np.concatenate([rows, np.asarray(er, np.int64)])
     cols = np.concatenate([cols, np.asarray(ec, np.int64)])
     return rows, cols
+
+
+def tf32_exact(x: np.ndarray) -> np.ndarray:
+    """float32 values with the low 13 fraction bits cleared, so every value is
+    exactly representable in TF32 and the tensor cores read it unchanged."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
+    return u.view(np.float32)

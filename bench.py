@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of libgemm on one GB300 (or N independent replicas).
+
+A step is one pass of the whole hot path: C = A*B at M = K = N = 4096 once in
+each precision mode -- exact FP32 on the CUDA cores, TF32 and BF16-input on the
+tensor cores -- on seeded synthetic inputs uniform on [0, 1) (the square
+sweep's largest size, the size the headline metric is quoted at).  Each GEMM
+counts 2*M*N*K floating-point operations, as the first page counts them
+("Matrix Multiplication -- Naive to Tiled", section 03).
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and a
+device synchronisation on both sides.  Before every GEMM a 256 MiB buffer is
+written to flush the 129 MB L2; each GEMM is bracketed by CUDA events on the
+stream it runs on, so the flush is outside the measured time.  ms_per_step is
+the mean over steps of the three GEMMs' event times.  The JSON line also
+carries the roofline of the dominant kernel, the fp64 oracle's throughput on
+the host cores (cpu_baseline), an end-to-end figure with host buffers, the SM
+clocks seen during the timed region and the number of library launches.
+
+``--impl reference`` times the fp64 CPU oracle instead (a bounded sample of
+rows of the same workload per step), on the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (FP32 and TF32/BF16) at N=4096, % of sm_103a peak"
+UNIT = "TFLOP/s"
+MODES = ("fp32", "tf32", "bf16")
+L2_FLUSH_BYTES = 256 << 20
+
+# GB300 facts used for the roofline denominators.
+NUM_SMS = 152
+SM_MAX_MHZ = 2070.0
+FP32_LANES_PER_SM = 128                      # FFMA lanes per SM (4 sub-partitions x 32)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+TF32_PER_BF16 = 1.1 / 2.25                   # nominal dense TF32 / BF16 tensor rates
+
+# DRAM traffic of one launch of the dominant kernel, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
+# kernel source it was taken on; reported as null once the source changes.
+TRAFFIC = {}
+
+
+def flops(M: int, K: int, N: int) -> float:
+    """Floating-point operations of one product: M*N outputs, K multiplies and K adds each."""
+    return 2.0 * M * N * K
+
+
+def tflops(M: int, K: int, N: int, seconds: float) -> float:
+    return flops(M, K, N) / seconds / 1e12
+
+
+def _measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+def fp32_ffma_peak(mhz: float = SM_MAX_MHZ) -> float:
+    """FP32 FFMA peak in TFLOP/s: SMs x lanes x 2 FLOP x clock."""
+    return NUM_SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def _src_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "accelerator_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _cpu_sample(A: np.ndarray, B: np.ndarray, fmt: str, rows: int):
+    """fp64 oracle on the first `rows` rows of C; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm(np.ascontiguousarray(A[:rows]), B, fmt=fmt)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(A: np.ndarray, B: np.ndarray, target_s: float = 12.0):
+    """The oracle as it stands, on all host cores, on a bounded sample of rows."""
+    import oracle
+    n = A.shape[0]
+    K, N = B.shape
+    cores = oracle.threads()
+    rows = 4
+    t = _cpu_sample(A, B, "f32", rows)
+    rows = int(max(4, min(n, rows * target_s / max(t, 1e-3))))
+    t = _cpu_sample(A, B, "f32", rows)
+    return {"value": tflops(rows, K, N, t), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {n} rows of C for the {n}x{K}x{N} FP32 input "
+                      f"(fp64 triple loop, {t:.1f} s)"}
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm."""
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from accelerator_gb300 import inputs
+    n = args.size
+    A, B = inputs.matrices(n, n, n, "u01")
+    fmt_inputs = {"fp32": (A, B, "f32"), "tf32": (A, B, "tf32"),
+                  "bf16": (inputs.bf16_bits(A), inputs.bf16_bits(B), "bf16")}
+    cores = oracle.threads()
+    # size each step so the whole run stays within a few minutes
+    t = _cpu_sample(A, B, "f32", 2)
+    per_step = max(1.0, min(8.0, 150.0 / (args.steps + args.warmup)))
+    rows = int(max(1, min(n, 2 * per_step / 3 / max(t, 1e-3))))
+
+    def step():
+        for m in MODES:
+            a, b, fmt = fmt_inputs[m]
+            oracle.gemm(np.ascontiguousarray(a[:rows]), b, fmt=fmt)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 3 * flops(rows, n, n) / dt / 1e12
+    sample = f"first {rows} of {n} rows of C per mode, 3 modes per step (fp64 triple loop)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"square GEMM M=K=N={n}, modes fp32+tf32+bf16, U[0,1) seed 42",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def run_libgemm(args):
+    import torch
+    import torch.distributed as dist
+    from accelerator_gb300 import binding, build, inputs
+
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    binding.lib()
+    dev = torch.device("cuda", local)
+    n = args.size
+    A, B = inputs.matrices(n, n, n, "u01")
+    a32, b32 = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    a16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16).to(dev)
+    b16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16).to(dev)
+    ops = {"fp32": (a32, b32, binding.FP32), "tf32": (a32, b32, binding.TF32),
+           "bf16": (a16, b16, binding.BF16)}
+    C = torch.zeros((n, n), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    f = flops(n, n, n)
+
+    def step(events=None):
+        for m in MODES:
+            a, b, mode = ops[m]
+            flush.zero_()
+            if events is not None:
+                events[m][0].record(stream)
+            binding.gemm(a, b, C, mode=mode, stream=stream)
+            if events is not None:
+                events[m][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.debug_status(stream) != binding.OK:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+
+    evs = [{m: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for m in MODES} for _ in range(args.steps)]
+    launches0 = binding.launch_count()
+    with ClockSampler(local) as clocks:
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for s in range(args.steps):
+            step(evs[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if ws > 1:
+            dist.barrier()
+    launches = binding.launch_count() - launches0
+    per_mode = {m: np.array([evs[s][m][0].elapsed_time(evs[s][m][1]) for s in range(args.steps)])
+                for m in MODES}
+    ms_step = float(np.mean(sum(per_mode[m] for m in MODES)))
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = ws * len(MODES) * f / (ms_step / 1e3) / 1e12
+    if binding.debug_status(stream) != binding.OK:
+        raise RuntimeError("a kernel reported a timeout during the timed region")
+    clk = clocks.summary()
+
+    # e2e: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.from_numpy(A).pin_memory()
+        hB = torch.from_numpy(B).pin_memory()
+        hA16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).pin_memory()
+        hB16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).pin_memory()
+        hC = torch.empty((n, n), dtype=torch.float32).pin_memory()
+        da, db = torch.empty_like(a32), torch.empty_like(b32)
+        da16 = torch.empty((n, n), dtype=torch.int16, device=dev)
+        db16 = torch.empty((n, n), dtype=torch.int16, device=dev)
+        host = {"fp32": (hA, hB, da, db, binding.FP32), "tf32": (hA, hB, da, db, binding.TF32),
+                "bf16": (hA16, hB16, da16, db16, binding.BF16)}
+        h2d = sum(host[m][0].numel() * host[m][0].element_size() * 2 for m in MODES)
+        d2h = len(MODES) * n * n * 4
+
+        def e2e_step():
+            for m in MODES:
+                ha, hb, xa, xb, mode = host[m]
+                xa.copy_(ha, non_blocking=True)
+                xb.copy_(hb, non_blocking=True)
+                if mode == binding.BF16:
+                    binding.gemm(xa.view(torch.bfloat16), xb.view(torch.bfloat16), C, mode=mode, stream=stream)
+                else:
+                    binding.gemm(xa, xb, C, mode=mode, stream=stream)
+                hC.copy_(C, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": ws * len(MODES) * f / (ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, bf16_peak, bf16_sus, src = _measured_peaks()
+    tf32_peak = bf16_peak * TF32_PER_BF16
+    sm_mhz = clk["sm_mhz"] if clk else None
+    modes_out = {}
+    for m in MODES:
+        ms = float(np.mean(per_mode[m]))
+        achieved = f / (ms / 1e3) / 1e12
+        if m == "fp32":
+            peak, bound, note = fp32_ffma_peak(), "alu", "FP32 FFMA: 152 SMs x 128 lanes x 2 x 2070 MHz"
+        elif m == "tf32":
+            peak, bound, note = tf32_peak, "tensor", f"{src} bf16 x nominal tf32/bf16 ratio"
+        else:
+            peak, bound, note = bf16_peak, "tensor", f"{src} bf16 burst"
+        modes_out[m] = {"ms_mean": ms, "ms_median": float(np.median(per_mode[m])),
+                        "tflops": achieved, "bound": bound, "peak": peak, "frac": achieved / peak,
+                        "peak_source": note}
+        if m == "fp32" and sm_mhz:
+            modes_out[m]["frac_at_observed_clock"] = achieved / fp32_ffma_peak(sm_mhz)
+    dom = max(MODES, key=lambda m: modes_out[m]["ms_mean"])
+    dom_file = "ffma_sgemm.cu" if dom == "fp32" else "tc_gemm.cu"
+    traffic = None
+    if dom_file in TRAFFIC and TRAFFIC[dom_file][0] == _src_hash(dom_file):
+        traffic = TRAFFIC[dom_file][1]
+    roofline = {"bound": modes_out[dom]["bound"], "achieved": modes_out[dom]["tflops"],
+                "peak": modes_out[dom]["peak"], "unit": "TFLOP/s",
+                "frac": modes_out[dom]["frac"], "traffic": traffic,
+                "kernel": dom_file, "per_launch_flops": f,
+                "peak_source": modes_out[dom]["peak_source"]}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(A, B)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32+tf32+bf16", "data": "synthetic",
+        "config": {"workload": f"square GEMM M=K=N={n}, one product per mode "
+                               "(fp32 FFMA, tf32 and bf16-input tcgen05), U[0,1) seed 42",
+                   "l2": "flushed before every GEMM (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{ws}"},
+        "modes": modes_out,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["libgemm", "reference"], default="libgemm")
+    p.add_argument("--size", type=int, default=4096)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_libgemm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

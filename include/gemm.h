@@ -1,0 +1,125 @@
+/*
+ * gemm.h -- C ABI of libgemm: dense C = A*B on one GB300 GPU (sm_103a).
+ *
+ * The operation.  With A of size M x K, B of size K x N and C of size M x N,
+ *     C_ij = sum over k = 0 .. K-1 of A_ik * B_kj
+ * ("Shared Memory Tiling for Matrix Multiplication", opening formula).  All
+ * three matrices are dense and row-major with no leading-dimension argument:
+ * A_ik is A[i*K + k], B_kj is B[k*N + j], C_ij is C[i*N + j] ("Matrix
+ * Multiplication -- Naive to Tiled", section 02).  C is overwritten, as that
+ * page's kernels store the finished sum; it is never read.
+ *
+ * Argument order (M, K, N) follows the kernel signature of that same section.
+ *
+ * Every pointer is a DEVICE pointer on the calling thread's current CUDA
+ * device; the caller owns all buffers and the stream, and the library frees
+ * nothing it did not allocate.  Every call is asynchronous: it validates its
+ * arguments on the host, enqueues its kernels on `stream` and returns.  Device
+ * errors of an earlier call surface through gemm_debug_status() or the
+ * caller's own synchronisation.  No call exits the process or traps the GPU.
+ *
+ * `stream` is a cudaStream_t (the pointer type is declared here so this header
+ * needs no CUDA header); NULL means the legacy default stream.
+ */
+#ifndef LIBGEMM_GEMM_H
+#define LIBGEMM_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the type behind cudaStream_t */
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+/* precision_mode values */
+enum gemm_mode {
+    /* A, B: const float*.  Exact binary32 arithmetic on the CUDA cores: every
+     * product-accumulate is one fused multiply-add rounded to nearest, k
+     * ascending for each C_ij. */
+    GEMM_FP32 = 0,
+    /* A, B: const float*.  Tensor cores (tcgen05, kind::tf32): the inputs are
+     * read as TF32 (sign, 8-bit exponent, top 10 fraction bits of each
+     * binary32), products are accumulated in binary32. */
+    GEMM_TF32 = 1,
+    /* A, B: const uint16_t* holding bfloat16 values (the caller rounds its
+     * data to bfloat16).  Tensor cores (tcgen05, kind::f16 with BF16
+     * inputs), binary32 accumulation. */
+    GEMM_BF16 = 2
+};
+
+/* Status codes returned by every entry point (0 = success). */
+enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* NULL pointer with a non-empty matrix, negative
+                                        dimension, unknown mode, C overlapping A or B,
+                                        or a size whose element count overflows int64 */
+    GEMM_ERR_MISALIGNED = 2,         /* pointer not aligned to its element size
+                                        (4 bytes for float, 2 bytes for bfloat16) */
+    GEMM_ERR_CUDA = 3,               /* a CUDA runtime call or kernel launch failed */
+    GEMM_ERR_NO_MEMORY = 4,          /* the stream-ordered scratch allocation failed */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 */
+    GEMM_ERR_TIMEOUT = 6             /* a bounded wait inside a kernel expired; the kernel
+                                        stopped early and its output is not valid */
+};
+
+/*
+ * C = A*B.
+ *   A               device pointer to M*K elements (float, or bfloat16 in GEMM_BF16)
+ *   B               device pointer to K*N elements (same element type as A)
+ *   C               device pointer to M*N floats; overwritten; must not overlap A or B
+ *   M, K, N         dimensions, each >= 0.  M == 0 or N == 0: nothing is done.
+ *                   K == 0: C is set to 0 (the empty sum).
+ *   precision_mode  one of enum gemm_mode
+ *   stream          stream to enqueue on
+ * Any alignment of element size or more is accepted.  When a tensor-core mode
+ * meets a row stride that is not a multiple of 16 bytes, or a base address
+ * that is not 16-byte aligned, the operand is first copied into a scratch
+ * buffer with a padded row stride; that buffer is taken from and returned to
+ * CUDA's stream-ordered allocator on `stream` inside the call.
+ * Returns GEMM_OK or an enum gemm_status code; on an error nothing is enqueued.
+ */
+GEMM_API int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
+         int precision_mode, struct CUstream_st* stream);
+
+/* Static, human-readable name of a status code ("unknown status" otherwise). */
+GEMM_API const char* gemm_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word, which kernels set when a bounded wait expires.  Returns GEMM_OK,
+ * GEMM_ERR_TIMEOUT, or GEMM_ERR_CUDA if the synchronisation itself failed.
+ */
+GEMM_API int gemm_debug_status(struct CUstream_st* stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+GEMM_API int gemm_version(void);
+
+/*
+ * Number of kernels this library has launched in this process, all devices
+ * and streams together.  Lets a benchmark count the launches in a timed
+ * region.
+ */
+GEMM_API int64_t gemm_launch_count(void);
+
+/*
+ * Self-test of the bounded wait used by the tensor-core kernel's pipeline:
+ * launches one block that waits on a barrier nothing will ever complete,
+ * giving up after `timeout_ns` nanoseconds (clamped to 1 us .. 2 s), and
+ * synchronises.  Returns GEMM_ERR_TIMEOUT when the wait expired and was
+ * reported as it should be, GEMM_OK if it was not (a defect), or a launch
+ * error.  Clears the error word before returning.  The GPU stays usable.
+ */
+GEMM_API int gemm_selftest_bounded_wait(int64_t timeout_ns, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBGEMM_GEMM_H */

@@ -27,3 +27,31 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def libgemm():
+    """The built library's binding (builds libgemm.so first if it is stale)."""
+    from accelerator_gb300 import binding, build
+    build.build()
+    binding.lib()
+    return binding
+
+
+class _OracleCache:
+    """Memoised oracle results keyed by the seeded-input recipe."""
+
+    def __init__(self):
+        self._full = {}
+
+    def full(self, key, A, B, fmt="f32"):
+        import oracle
+        k = (key, fmt)
+        if k not in self._full:
+            self._full[k] = oracle.gemm(A, B, fmt=fmt)
+        return self._full[k]
+
+
+@pytest.fixture(scope="session")
+def oracle_cache():
+    return _OracleCache()

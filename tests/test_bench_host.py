@@ -1,0 +1,32 @@
+"""Host-side logic of bench.py, CPU only: the rate formula against the pages'
+printed table, the roofline peak arithmetic and the command line."""
+import pytest
+
+import bench
+from golden_io import page_gflops
+
+
+def test_flop_count_matches_page():
+    # "Matrix Multiplication -- Naive to Tiled", section 03: 2.15 billion at N = 1024
+    assert round(bench.flops(1024, 1024, 1024) / 1e9, 2) == 2.15
+    # "From 306 ms to 86 ms": 16.8 million elements of C at N = 4096
+    assert round(4096 * 4096 / 1e6, 1) == 16.8
+
+
+@pytest.mark.parametrize("row", page_gflops(), ids=lambda r: f"N{r[0]}-{r[1]}ms")
+def test_rate_formula_reproduces_page_table(row):
+    n, ms, gflops, dec = row
+    half = 0.5 * 10.0 ** -dec            # the printed time is rounded to `dec` decimals
+    lo = bench.tflops(n, n, n, (ms + half) / 1e3) * 1e3
+    hi = bench.tflops(n, n, n, (ms - half) / 1e3) * 1e3
+    assert lo - 0.5 <= gflops <= hi + 0.5
+
+
+def test_fp32_peak_arithmetic():
+    assert abs(bench.fp32_ffma_peak() - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+    assert abs(bench.fp32_ffma_peak(1485.0) / bench.fp32_ffma_peak() - 1485 / 2070) < 1e-12
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "1"])

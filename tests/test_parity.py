@@ -1,0 +1,95 @@
+"""GPU parity: libgemm through its C ABI against the fp64 oracle.
+
+Workloads are the seeded synthetic inputs of the pages' studies:
+  * 256^3 and 1024^3 with entries uniform on [0, 1);
+  * the ragged 1000 x 777 x 1500 shape with entries uniform on [-1, 1), and
+    the same shape with integers in [-4, 4] (exact in every mode: bit-exact);
+  * the square sweep N = 128 .. 4096 (full oracle up to 1024, then 4096+
+    sampled entries and the sum-of-all-elements identity);
+  * 8192^3 on the tensor-core modes, uniform on [-1, 1).
+Every element must satisfy |C - Cref| <= tol * S_ij; C is poisoned with NaN
+before each launch so an unwritten element fails.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from accelerator_gb300 import inputs
+from checks import TOL, TOL_SAME_INPUTS, assert_exact, assert_sum, assert_within
+from gpu_util import oracle_inputs, run
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["fp32", "tf32", "bf16"]
+
+
+def _full_case(libgemm, oracle_cache, M, K, N, dist, mode):
+    A, B = inputs.matrices(M, K, N, dist)
+    C = run(libgemm, A, B, mode)
+    Cref, S = oracle_cache.full((M, K, N, dist), A, B)
+    worst = assert_within(C, Cref, S, TOL[mode], f"{mode} {M}x{K}x{N} {dist}")
+    return A, B, C, worst
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_square_256_u01(libgemm, oracle_cache, mode):
+    _full_case(libgemm, oracle_cache, 256, 256, 256, "u01", mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_square_1024_u01(libgemm, oracle_cache, mode):
+    _full_case(libgemm, oracle_cache, 1024, 1024, 1024, "u01", mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_ragged_1000x777x1500_pm1(libgemm, oracle_cache, mode):
+    _full_case(libgemm, oracle_cache, 1000, 777, 1500, "pm1", mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_ragged_integers_bit_exact(libgemm, oracle_cache, mode):
+    # |C| <= 777 * 16 < 2**24 and every partial sum is an integer: exact in binary32
+    A, B = inputs.matrices(1000, 777, 1500, "int4")
+    C = run(libgemm, A, B, mode)
+    Cref, _ = oracle_cache.full((1000, 777, 1500, "int4"), A, B)
+    assert_exact(C, Cref, f"{mode} integers")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n", [128, 512])
+def test_sweep_small_full(libgemm, oracle_cache, mode, n):
+    _full_case(libgemm, oracle_cache, n, n, n, "u01", mode)
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_same_inputs_diagnostic(libgemm, mode):
+    """Tensor path against the oracle fed the very values the tensor cores
+    read (TF32-exact or BF16 values): only binary32 accumulation differs."""
+    A, B = inputs.matrices(512, 1000, 384, "pm1", seed=77)
+    if mode == "tf32":
+        A, B = inputs.tf32_exact(A), inputs.tf32_exact(B)
+    C = run(libgemm, A, B, mode)
+    a, b, fmt = oracle_inputs(A, B, mode)
+    Cref, S = oracle.gemm(a, b, fmt=fmt)
+    assert_within(C, Cref, S, TOL_SAME_INPUTS, f"{mode} same-inputs")
+
+
+def _sampled_case(libgemm, M, K, N, dist, mode, n=4096):
+    A, B = inputs.matrices(M, K, N, dist)
+    C = run(libgemm, A, B, mode)
+    rows, cols = inputs.sample_indices(M, N, n=n)
+    cref, s = oracle.dot(A, B, rows, cols)
+    assert_within(C[rows, cols], cref, s, TOL[mode], f"{mode} {M}x{K}x{N} sampled")
+    total, abs_total = oracle.total(A, B)
+    assert_sum(C, total, abs_total, TOL[mode], f"{mode} {M}x{K}x{N} sum")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n", [2048, 4096])
+def test_sweep_large_sampled(libgemm, mode, n):
+    _sampled_case(libgemm, n, n, n, "u01", mode)
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_large_8192_sampled(libgemm, mode):
+    _sampled_case(libgemm, 8192, 8192, 8192, "pm1", mode)
