@@ -22,6 +22,7 @@ ERR_CUDA = 3
 ERR_NO_MEMORY = 4
 ERR_UNSUPPORTED_DEVICE = 5
 ERR_TIMEOUT = 6
+ERR_SCRATCH_LIMIT = 7
 
 # Every entry point include/gemm.h declares, with its ctypes signature.
 _i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -32,6 +33,7 @@ SIGNATURES = {
     "gemm_version": (_int, []),
     "gemm_launch_count": (_i64, []),
     "gemm_selftest_bounded_wait": (_int, [_i64, _vp]),
+    "gemm_tf32_noalloc": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
 }
 
 _lock = threading.Lock()

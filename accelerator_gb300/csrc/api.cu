@@ -160,6 +160,28 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
 
 }  // namespace
 
+// Internal hooks for other translation units of this library (declared in
+// kernels.h); they reuse the set-up above without changing it.
+namespace libgemm {
+
+int device_setup(int* num_sms, unsigned** err) {
+    DeviceState* st = nullptr;
+    const int rc = device_state(&st);
+    if (rc != GEMM_OK) return rc;
+    *num_sms = st->num_sms;
+    *err = st->err;
+    return GEMM_OK;
+}
+
+int encode_tensor_map_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols,
+                         int64_t ld, int box_cols, int box_rows) {
+    return encode_2d(map, ptr, es, rows, cols, ld, box_cols, box_rows);
+}
+
+void count_launch() { g_launches++; }
+
+}  // namespace libgemm
+
 extern "C" {
 
 int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
@@ -216,6 +238,8 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_NO_MEMORY: return "scratch allocation failed";
     case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
     case GEMM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case GEMM_ERR_SCRATCH_LIMIT:
+        return "the product needs more scratch than the no-allocation entry point's static buffer";
     default: return "unknown status";
     }
 }

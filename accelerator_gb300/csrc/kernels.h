@@ -40,4 +40,15 @@ cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t c
 cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
+// ---- host-side hooks of the C ABI (api.cu) ----
+// Per-device set-up of the library (device check, kernel attributes, error
+// word); returns a gemm_status code.
+int device_setup(int* num_sms, unsigned** err);
+// Tensor map over a rows x cols row-major matrix (row stride ld elements),
+// box box_cols x box_rows, 128-byte swizzle, zero fill; gemm_status code.
+int encode_tensor_map_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols,
+                         int64_t ld, int box_cols, int box_rows);
+// Add one to the library's launch counter.
+void count_launch();
+
 }  // namespace libgemm

@@ -65,8 +65,10 @@ enum gemm_status {
     GEMM_ERR_CUDA = 3,               /* a CUDA runtime call or kernel launch failed */
     GEMM_ERR_NO_MEMORY = 4,          /* the stream-ordered scratch allocation failed */
     GEMM_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 */
-    GEMM_ERR_TIMEOUT = 6             /* a bounded wait inside a kernel expired; the kernel
+    GEMM_ERR_TIMEOUT = 6,            /* a bounded wait inside a kernel expired; the kernel
                                         stopped early and its output is not valid */
+    GEMM_ERR_SCRATCH_LIMIT = 7       /* gemm_tf32_noalloc: the product needs more scratch
+                                        than GEMM_NOALLOC_SCRATCH_BYTES */
 };
 
 /*
@@ -117,6 +119,46 @@ GEMM_API int64_t gemm_launch_count(void);
  * error.  Clears the error word before returning.  The GPU stays usable.
  */
 GEMM_API int gemm_selftest_bounded_wait(int64_t timeout_ns, struct CUstream_st* stream);
+
+/*
+ * gemm_tf32_noalloc -- the GEMM_TF32 product without allocating device memory.
+ *
+ * The pages have no counterpart for this entry point; it is a service of this
+ * library.  gemm() in GEMM_TF32 needs scratch (a transposed copy of B, and a
+ * re-strided copy of A when A's rows are not 16-byte multiples) and takes it
+ * from CUDA's stream-ordered allocator.  Some callers cannot allow that: a
+ * host application that has reserved the device memory for its own pool, so
+ * an allocation would fail or eat into its budget; or a latency-critical
+ * loop where an allocation may stall or fail at a bad moment.  This entry
+ * point uses instead one static device buffer of GEMM_NOALLOC_SCRATCH_BYTES,
+ * compiled into the library: it never calls cudaMalloc, cudaMallocAsync,
+ * cudaFree or any allocating routine.
+ *
+ * Arguments and results are those of gemm() with precision_mode GEMM_TF32:
+ * A, B, C device pointers (float), row-major, C overwritten, asynchronous on
+ * `stream`, the same kernels and therefore the same values as gemm().
+ *
+ * Limit: 4 * N * roundup(K, 4) bytes (rounded up to 256) for B^T, plus, when A
+ * is not 16-byte aligned or K % 4 != 0, 4 * M * roundup(K, 4) bytes (rounded
+ * up to 256) for A, must not exceed GEMM_NOALLOC_SCRATCH_BYTES (64 MiB: for
+ * example K = N = 4096 with an aligned A).  Larger products return
+ * GEMM_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *
+ * Set-up: the first call on a device (that device current) loads the buffer
+ * and looks up its device address; make that first call before any stream
+ * capture.  Every device that has made a call holds the buffer until the
+ * process exits.
+ *
+ * Sharing: every call on a device uses the same buffer, which keeps the last
+ * call's contents (nothing in it needs to start at zero: every byte a call
+ * reads was written by that call).  Calls whose kernels overlap on the GPU --
+ * on different streams, or from different threads -- race on the buffer and
+ * give wrong results: order them on one stream, or synchronise between them.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (64ll * 1024 * 1024)
+
+GEMM_API int gemm_tf32_noalloc(const float* A, const float* B, float* C, int64_t M, int64_t K,
+                               int64_t N, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol(libgemm):
 
 
 def test_status_strings(libgemm):
-    for code in range(7):
+    for code in range(8):
         s = libgemm.status_string(code)
         assert s and s != "unknown status"
     assert libgemm.status_string(99) == "unknown status"
