@@ -6,7 +6,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "kernels.h"
 
 namespace {
@@ -24,6 +24,10 @@ struct DeviceState {
     int status = GEMM_OK;
     int num_sms = 0;
     unsigned* err = nullptr;
+    // Scratch comes from this pool, stream-ordered.  It keeps what it has
+    // reserved (release threshold: never), so repeated calls reuse memory
+    // instead of mapping it afresh after every synchronisation.
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -35,6 +39,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+bool make_pool(int dev, cudaMemPool_t* pool) {
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(pool, &props) != cudaSuccess) return false;
+    uint64_t keep = UINT64_MAX;
+    return cudaMemPoolSetAttribute(*pool, cudaMemPoolAttrReleaseThreshold, &keep) == cudaSuccess;
+}
 
 // Per-device set-up, once: device check, SM count, error word address,
 // kernel attributes, and the driver's tensor-map encoder.
@@ -55,6 +70,8 @@ int device_state(DeviceState** out) {
             st.status = GEMM_ERR_UNSUPPORTED_DEVICE;
         } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_error_word) != cudaSuccess ||
                    ffma_setup() != cudaSuccess || tc_setup() != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (!make_pool(dev, &st.pool)) {
             st.status = GEMM_ERR_CUDA;
         } else if (!g_encode) {
             cudaDriverEntryPointQueryResult q;
@@ -95,6 +112,39 @@ int encode_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t c
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
+              DeviceState* st, cudaStream_t stream) {
+    const bool b_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+    const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    const FfmaPlan plan = ffma_plan((int)M, (int)N, (int)K, st->num_sms);
+    void* scratch = nullptr;
+    float* partial = nullptr;
+    unsigned* counters = nullptr;
+    if (plan.split_tiles > 0) {
+        const int64_t pb = round_up(plan.partial_bytes, 256), cb = round_up(plan.counter_bytes, 256);
+        if (cudaMallocFromPoolAsync(&scratch, (size_t)(pb + cb), st->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NO_MEMORY;
+        }
+        partial = static_cast<float*>(scratch);
+        counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(scratch) + pb);
+        // the counters must start at 0 (0.0f has all bits clear)
+        if (launch_fill_zero(reinterpret_cast<float*>(counters), cb / 4, stream) != cudaSuccess) {
+            cudaFreeAsync(scratch, stream);
+            return GEMM_ERR_CUDA;
+        }
+        g_launches++;
+    }
+    int rc = GEMM_OK;
+    if (launch_ffma_sgemm(A, B, C, (int)M, (int)N, (int)K, b_vec, c_vec, plan, partial, counters,
+                          stream) != cudaSuccess)
+        rc = GEMM_ERR_CUDA;
+    else
+        g_launches++;
+    if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
+    return rc;
+}
+
 int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
                      int64_t N, DeviceState* st, cudaStream_t stream) {
     const int es = mode == TcMode::kBF16 ? 2 : 4;
@@ -117,7 +167,8 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
     const void* a_use = A;
     const void* b_use = B;
     if (a_bytes + b_bytes > 0) {
-        if (cudaMallocAsync(&scratch, (size_t)(a_bytes + b_bytes), stream) != cudaSuccess) {
+        if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes), st->pool, stream) !=
+            cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_NO_MEMORY;
         }
@@ -216,15 +267,9 @@ int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N
         g_launches++;
         return GEMM_OK;
     }
-    if (precision_mode == GEMM_FP32) {
-        const bool b_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
-        const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
-        if (launch_ffma_sgemm(static_cast<const float*>(A), static_cast<const float*>(B), C, (int)M,
-                              (int)N, (int)K, b_vec, c_vec, stream) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        g_launches++;
-        return GEMM_OK;
-    }
+    if (precision_mode == GEMM_FP32) return ffma_gemm(static_cast<const float*>(A),
+                                                      static_cast<const float*>(B), C, M, K, N, st,
+                                                      stream);
     return tensor_core_gemm(precision_mode == GEMM_BF16 ? TcMode::kBF16 : TcMode::kTF32, A, B, C,
                             M, K, N, st, stream);
 }

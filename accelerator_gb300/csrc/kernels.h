@@ -11,9 +11,19 @@ namespace libgemm {
 // ---- exact-FP32 CUDA-core GEMM (ffma_sgemm.cu) ----
 // b_vec: B rows may be copied 16 bytes at a time (N % 4 == 0, B 16-byte aligned).
 // c_vec: C rows may be stored 16 bytes at a time (N % 4 == 0, C 16-byte aligned).
+// Work split: the first dp_tiles tiles whole, the last split_tiles tiles each
+// in `splits` K ranges whose partials (partial_bytes of scratch) are summed by
+// the last CTA of the tile (counter_bytes of zeroed counters).
+struct FfmaPlan {
+    int64_t tiles, dp_tiles, split_tiles;
+    int splits;
+    int64_t partial_bytes, counter_bytes;
+};
 cudaError_t ffma_setup();
+FfmaPlan ffma_plan(int M, int N, int K, int num_sms);
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
-                              bool b_vec, bool c_vec, cudaStream_t stream);
+                              bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
+                              unsigned* counters, cudaStream_t stream);
 
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
 enum class TcMode { kBF16, kTF32 };

@@ -18,7 +18,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "kernels.h"
 
 namespace {

@@ -37,6 +37,17 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool 
                  "l"(__cvta_generic_to_global(src)), "r"(pred ? 16 : 0)
                  : "memory");
 }
+// Unconditional forms, for copies known to be in range.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
