@@ -52,7 +52,10 @@ TF32_PER_BF16 = 1.1 / 2.25                   # nominal dense TF32 / BF16 tensor 
 # DRAM traffic of one launch of the dominant kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
 # kernel source it was taken on; reported as null once the source changes.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/ffma_sgemm_fp32_4096.md: 332.0 MB read + 55.6 MB written
+    "ffma_sgemm.cu": ("53836c88ddffda8674c6bbbc2fc5a2713edbb340ae87d8bef88ae95a4cb5892d", 387.6e6),
+}
 
 
 def flops(M: int, K: int, N: int) -> float:
@@ -86,57 +89,108 @@ def _src_hash(name: str) -> str:
 
 # --------------------------------------------------------------------------
 # clocks during the timed region
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.path = None
+    """Samples the SM clock and the clock-event reasons every few ms in a
+    thread while the timed region runs, through NVML (libnvidia-ml, read-only
+    queries).  Falls back to nvidia-smi when NVML cannot be loaded."""
+
+    def __init__(self, torch_device_index: int, period_s: float = 0.004):
+        self.index = torch_device_index
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.index).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(handle)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+            self.max_mhz = float(mx.value)
+        self._nvml, self._handle = lib, handle
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk, why = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = why.value if get_reasons(h, ctypes.byref(why)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
         try:
-            import tempfile
-            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
-            os.close(fd)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index),
-                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self._open_nvml()
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         except Exception:
-            self.proc = None
+            self._nvml = None
+            try:
+                import tempfile
+                fd, path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+                os.close(fd)
+                self._smi = (path, subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=open(path, "w"), stderr=subprocess.DEVNULL))
+            except Exception:
+                self._smi = None
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self._smi is not None:
+            path, proc = self._smi
+            proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                proc.wait(timeout=5)
             except Exception:
-                self.proc.kill()
+                proc.kill()
+            with open(path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    try:
+                        self.samples.append((float(parts[0]), int(parts[2], 16)))
+                        self.max_mhz = float(parts[1])
+                    except (ValueError, IndexError):
+                        continue
+            os.unlink(path)
 
     def summary(self):
-        if not self.path or not os.path.exists(self.path):
+        if not self.samples:
             return None
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 7:
-                    continue
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
-                except ValueError:
-                    continue
-        os.unlink(self.path)
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        return {"sm_mhz": float(np.median([r[0] for r in rows])),
-                "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({name for _, r in self.samples for bit, name in _REASONS.items() if r & bit})
+        return {"sm_mhz": float(np.median([c for c, _ in self.samples])),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
 # --------------------------------------------------------------------------
@@ -155,15 +209,18 @@ def _cpu_sample(A: np.ndarray, B: np.ndarray, fmt: str, rows: int):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(A: np.ndarray, B: np.ndarray, target_s: float = 12.0):
-    """The oracle as it stands, on all host cores, on a bounded sample of rows."""
+def cpu_baseline(A: np.ndarray, B: np.ndarray, target_s: float = 15.0):
+    """The oracle as it stands, on all host cores, on a bounded sample: the
+    first rows of C, as many as take about target_s seconds."""
     import oracle
     n = A.shape[0]
     K, N = B.shape
     cores = oracle.threads()
-    rows = 4
-    t = _cpu_sample(A, B, "f32", rows)
-    rows = int(max(4, min(n, rows * target_s / max(t, 1e-3))))
+    t1 = _cpu_sample(A, B, "f32", 16)
+    t2 = _cpu_sample(A, B, "f32", 48)
+    per_row = max((t2 - t1) / 32, 1e-6)
+    fixed = max(t1 - 16 * per_row, 0.0)
+    rows = int(max(16, min(n, (target_s - fixed) / per_row)))
     t = _cpu_sample(A, B, "f32", rows)
     return {"value": tflops(rows, K, N, t), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {n} rows of C for the {n}x{K}x{N} FP32 input "
@@ -239,7 +296,7 @@ def run_libgemm(args):
     f = flops(n, n, n)
 
     def step(events=None):
-        for m in MODES:
+        for m in args.modes:
             a, b, mode = ops[m]
             flush.zero_()
             if events is not None:
@@ -255,7 +312,7 @@ def run_libgemm(args):
         raise RuntimeError("a kernel reported a timeout during warm-up")
 
     evs = [{m: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for m in MODES} for _ in range(args.steps)]
+            for m in args.modes} for _ in range(args.steps)]
     launches0 = binding.launch_count()
     with ClockSampler(local) as clocks:
         if ws > 1:
@@ -270,13 +327,13 @@ def run_libgemm(args):
             dist.barrier()
     launches = binding.launch_count() - launches0
     per_mode = {m: np.array([evs[s][m][0].elapsed_time(evs[s][m][1]) for s in range(args.steps)])
-                for m in MODES}
-    ms_step = float(np.mean(sum(per_mode[m] for m in MODES)))
+                for m in args.modes}
+    ms_step = float(np.mean(sum(per_mode[m] for m in args.modes)))
     if ws > 1:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
-    value = ws * len(MODES) * f / (ms_step / 1e3) / 1e12
+    value = ws * len(args.modes) * f / (ms_step / 1e3) / 1e12
     if binding.debug_status(stream) != binding.OK:
         raise RuntimeError("a kernel reported a timeout during the timed region")
     clk = clocks.summary()
@@ -294,11 +351,11 @@ def run_libgemm(args):
         db16 = torch.empty((n, n), dtype=torch.int16, device=dev)
         host = {"fp32": (hA, hB, da, db, binding.FP32), "tf32": (hA, hB, da, db, binding.TF32),
                 "bf16": (hA16, hB16, da16, db16, binding.BF16)}
-        h2d = sum(host[m][0].numel() * host[m][0].element_size() * 2 for m in MODES)
-        d2h = len(MODES) * n * n * 4
+        h2d = sum(host[m][0].numel() * host[m][0].element_size() * 2 for m in args.modes)
+        d2h = len(args.modes) * n * n * 4
 
         def e2e_step():
-            for m in MODES:
+            for m in args.modes:
                 ha, hb, xa, xb, mode = host[m]
                 xa.copy_(ha, non_blocking=True)
                 xb.copy_(hb, non_blocking=True)
@@ -318,7 +375,7 @@ def run_libgemm(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
-        e2e = {"value": ws * len(MODES) * f / (ms / 1e3) / 1e12, "unit": UNIT,
+        e2e = {"value": ws * len(args.modes) * f / (ms / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
     if rank != 0:
@@ -330,7 +387,7 @@ def run_libgemm(args):
     tf32_peak = bf16_peak * TF32_PER_BF16
     sm_mhz = clk["sm_mhz"] if clk else None
     modes_out = {}
-    for m in MODES:
+    for m in args.modes:
         ms = float(np.mean(per_mode[m]))
         achieved = f / (ms / 1e3) / 1e12
         if m == "fp32":
@@ -344,7 +401,7 @@ def run_libgemm(args):
                         "peak_source": note}
         if m == "fp32" and sm_mhz:
             modes_out[m]["frac_at_observed_clock"] = achieved / fp32_ffma_peak(sm_mhz)
-    dom = max(MODES, key=lambda m: modes_out[m]["ms_mean"])
+    dom = max(args.modes, key=lambda m: modes_out[m]["ms_mean"])
     dom_file = "ffma_sgemm.cu" if dom == "fp32" else "tc_gemm.cu"
     traffic = None
     if dom_file in TRAFFIC and TRAFFIC[dom_file][0] == _src_hash(dom_file):
@@ -390,7 +447,13 @@ def main(argv=None):
     p.add_argument("--size", type=int, default=4096)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--modes", default=",".join(MODES),
+                   help="comma-separated subset of fp32,tf32,bf16 (default: all three; "
+                        "a subset is for profiling single kernels, not a bench line)")
     args = p.parse_args(argv)
+    args.modes = tuple(m for m in MODES if m in args.modes.split(","))
+    if not args.modes:
+        p.error("--modes selects none of fp32, tf32, bf16")
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
