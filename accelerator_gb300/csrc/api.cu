@@ -192,15 +192,27 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
         }
     }
 
+    // The 2-SM kernel (CTA pairs) when the device can hold pair clusters; each
+    // CTA of a pair loads half of the B tile, so a K-major B box is half as tall.
+    const bool pairs = tc_max_pairs() > 0;
+    const int b_rows = pairs ? shape.block_n / 2 : shape.block_n;
     CUtensorMap map_a, map_b;
     int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m);
     if (rc == GEMM_OK)
-        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, shape.block_n)
+        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows)
                        : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems);
+    const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
+    CUtensorMap map_c;
+    const bool c_tma = pairs && c_vec && rc == GEMM_OK &&
+                       encode_2d(&map_c, C, 4, M, N, N, 32, 32) == GEMM_OK;
     if (rc == GEMM_OK) {
-        const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
-        if (launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
-                           st->num_sms, st->err, kWaitLimitNs, stream) != cudaSuccess)
+        const cudaError_t e =
+            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
+                                        (int)M, (int)N, (int)K, c_vec, st->err, kWaitLimitNs, stream)
+                  : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
+                                   st->num_sms, st->err, kWaitLimitNs, stream);
+        if (e != cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
             g_launches++;

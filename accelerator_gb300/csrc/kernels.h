@@ -34,6 +34,17 @@ struct TcShape {
 };
 TcShape tc_shape(TcMode mode);
 cudaError_t tc_setup();
+// Clusters of two CTAs of the 2-SM kernel that fit at once (0: unavailable).
+int tc_max_pairs();
+// 2-SM (CTA pair) kernel: BF16 with B MN-major, or TF32 with B^T K-major.
+// Its TMA boxes: A as for the 1-SM kernel; B boxes of k_elems rows x 128
+// bytes (MN-major) or 128 rows x 128 bytes (K-major), i.e. block_n / 2 wide.
+// map_c (may be null): C as a 2-D fp32 tensor, box 32 x 32, 128-byte swizzle,
+// for TMA stores of the epilogue; without it C is stored by the threads.
+cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+                                const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
+                                int N, int K, bool c_vec, unsigned* err, uint64_t limit_ns,
+                                cudaStream_t stream);
 // b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,

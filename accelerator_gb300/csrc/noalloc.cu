@@ -121,12 +121,21 @@ extern "C" int gemm_tf32_noalloc(const float* A, const float* B, float* C, int64
     const TcShape shape = tc_shape(TcMode::kTF32);
     CUtensorMap map_a, map_b;
     rc = encode_tensor_map_2d(&map_a, a_use, 4, M, K, pad_a ? ld : K, shape.k_elems, shape.block_m);
-    if (rc == GEMM_OK) rc = encode_tensor_map_2d(&map_b, bt, 4, N, K, ld, shape.k_elems, shape.block_n);
+    const bool pairs = tc_max_pairs() > 0;   // the same kernel choice as gemm()
+    if (rc == GEMM_OK)
+        rc = encode_tensor_map_2d(&map_b, bt, 4, N, K, ld, shape.k_elems,
+                                  pairs ? shape.block_n / 2 : shape.block_n);
     if (rc != GEMM_OK) return rc;
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
-    if (launch_tc_gemm(TcMode::kTF32, true, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec, num_sms,
-                       err, kWaitLimitNs, stream) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+    CUtensorMap map_c;
+    const bool c_tma =
+        pairs && c_vec && encode_tensor_map_2d(&map_c, C, 4, M, N, N, 32, 32) == GEMM_OK;
+    const cudaError_t e =
+        pairs ? launch_tc_gemm_pair(TcMode::kTF32, true, map_a, map_b, c_tma ? &map_c : nullptr, C,
+                                    (int)M, (int)N, (int)K, c_vec, err, kWaitLimitNs, stream)
+              : launch_tc_gemm(TcMode::kTF32, true, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
+                               num_sms, err, kWaitLimitNs, stream);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
     count_launch();
     return GEMM_OK;
 }

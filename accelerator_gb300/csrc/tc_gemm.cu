@@ -276,6 +276,272 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// 2-SM version: a cluster of two CTAs (a "pair") computes a 256 x 256 tile
+// with tcgen05.mma.cta_group::2 (M = 256, N = 256).  Each CTA holds its own
+// 128 rows of A and its own 128 columns of B in shared memory, so per MMA an
+// SM reads 4 KB of A and 4 KB of B instead of 4 + 8, and its TMA writes half
+// the B bytes: the shared-memory traffic per MMA cycle that limits the 1-SM
+// kernel is cut by a third.  The accumulator is split by rows: each CTA's
+// TMEM holds its 128 rows x 256 fp32 columns, and each CTA's epilogue stores
+// its own rows.
+//
+// Roles (both CTAs run the same code):
+//   warp 0  producer: loads this CTA's A rows and B columns of each K slab;
+//           the copies of BOTH CTAs complete on the leader's "full" barrier,
+//           which the leader's producer arms with the bytes of the pair.
+//   warp 1  allocates TMEM for the pair (collectively with the peer's warp 1);
+//           in the leader (cluster rank 0) one thread issues the MMAs and
+//           commits them to the "empty" barriers of both CTAs (multicast),
+//           and to both CTAs' accumulator-full barriers after a tile.
+//   warps 2-5  epilogue of this CTA's rows; each warp then arrives on the
+//           leader's accumulator-empty barrier (count 8: 4 warps x 2 CTAs).
+constexpr int kPStages = 6;
+// How the pair kernel writes C: TMA stores from swizzled staging (16-byte
+// aligned C rows), 16-byte vector stores, or 4-byte stores.
+enum : int { kStoreScalar = 0, kStoreVec = 1, kStoreTma = 2 };
+constexpr int kPHalfN = kBN / 2;                     // B columns held per CTA
+constexpr int kPABytes = kBM * kSlabBytes;           // 16 KB
+constexpr int kPBBytes = kPHalfN * kSlabBytes;       // 16 KB
+constexpr int kPStageBytes = kPABytes + kPBBytes;    // 32 KB
+// Epilogue staging: per epilogue warp two 32 x 32 fp32 blocks (4 KB each),
+// laid out with the 128-byte swizzle the TMA store expects.
+constexpr int kPStageCBytes = 4 * 2 * 32 * 32 * 4;   // 32 KB
+constexpr size_t kPSmemBytes =
+    size_t(kPStages) * kPStageBytes + kPStageCBytes + 1024 + 256;
+
+template <TcMode MODE, bool kBKMajor>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_c, float* __restrict__ C, int M,
+                        int N, int K, int pairs_m, int tiles_n, int c_mode, unsigned* err,
+                        uint64_t limit_ns) {
+    using T = Traits<MODE>;
+    constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
+    constexpr int kUmmaK = 32 / T::kEs;                   // K per MMA: 16 / 8
+    constexpr int kMmaPerStage = kKElems / kUmmaK;        // 4
+    constexpr int kBoxN = kSlabBytes / T::kEs;            // N per MN-major B box: 64 (bf16)
+    constexpr int kBoxes = kPHalfN / kBoxN;               // 2 (bf16)
+    constexpr uint32_t kBoxBytes = kKElems * kSlabBytes;  // 8 KB (bf16)
+    constexpr uint32_t kIdesc = make_idesc(T::kFormat, 2 * kBM, kBN, false, !kBKMajor);
+    constexpr uint32_t kPairTx = 2u * kPStageBytes;       // bytes the leader's full barrier awaits
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;                                   // kPStages x kPABytes
+    const uint32_t sB = base + kPStages * kPABytes;             // kPStages x kPBBytes
+    const uint32_t sC = base + kPStages * kPStageBytes;         // epilogue staging
+    uint8_t* ctrl = gbase + kPStages * kPStageBytes + kPStageCBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ctrl);
+    // full[0..S), empty[S..2S), acc_full[2S..2S+2), acc_empty[2S+2..2S+4), drain[2S+4]
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kPStages;
+    const uint32_t accf0 = full0 + 16 * kPStages, acce0 = accf0 + 16, drain_bar = acce0 + 16;
+    volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ctrl + 8 * (2 * kPStages + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + 8 * (2 * kPStages + 5) + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();            // 0: leader, 1: peer
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 2 * 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_holder)), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers and TMEM exist before anyone signals the other
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int npairs = pairs_m * tiles_n;
+    const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int nk = (K + kKElems - 1) / kKElems;
+    // the pair tile p covers rows pm*256 .. +255 and columns pn*256 .. +255
+    auto coords = [&](int p, int& m0, int& n0) {
+        const int per_group = kGroupM * tiles_n;
+        const int group = p / per_group;
+        const int first_m = group * kGroupM;
+        const int gsize = min(pairs_m - first_m, kGroupM);
+        m0 = (first_m + (p % per_group) % gsize) * (2 * kBM);
+        n0 = ((p % per_group) / gsize) * kBN;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            tma_prefetch_map(&map_a);
+            tma_prefetch_map(&map_b);
+            const uint32_t full_leader0 = mapa_shared(full0, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t last_phase[kPStages];
+            bool used[kPStages];
+            for (int s = 0; s < kPStages; ++s) used[s] = false, last_phase[s] = 0;
+            for (int p = cluster_id; p < npairs; p += nclusters) {
+                int m0, n0;
+                coords(p, m0, n0);
+                const int my_m0 = m0 + (int)rank * kBM, my_n0 = n0 + (int)rank * kPHalfN;
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, err, limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, kPairTx);
+                    const uint32_t fb = full_leader0 + 8 * stage;
+                    tma_load_2d_pair(sA + stage * kPABytes, &map_a, fb, kb * kKElems, my_m0);
+                    if constexpr (kBKMajor) {
+                        tma_load_2d_pair(sB + stage * kPBBytes, &map_b, fb, kb * kKElems, my_n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kBoxes; ++j)
+                            tma_load_2d_pair(sB + stage * kPBBytes + j * kBoxBytes, &map_b, fb,
+                                             my_n0 + j * kBoxN, kb * kKElems);
+                    }
+                    used[stage] = true;
+                    last_phase[stage] = phase;
+                    if (++stage == kPStages) stage = 0, phase ^= 1u;
+                }
+                if (!ok) break;
+            }
+            // Each copy issued here must have landed before the CTA exits: a
+            // slot's copy has been consumed once the MMAs that read it freed it.
+            for (int s = 0; s < kPStages; ++s)
+                if (used[s] && !drain_wait(empty0 + 8 * s, last_phase[s], limit_ns))
+                    atomicOr(err, kErrTimeout);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader CTA only) ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int lt = 0;
+            for (int p = cluster_id; p < npairs; p += nclusters, ++lt) {
+                const int buf = lt & 1;
+                const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait(acce0 + 8 * buf, use_parity ^ 1u, abort_flag, err, limit_ns)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kAccCols);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err, limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_tile = sA + stage * kPABytes;
+                    const uint32_t b_tile = sB + stage * kPBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(a_tile + kk * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            kBKMajor ? smem_desc_sw128(b_tile + kk * 32, 16, 1024)
+                                     : smem_desc_sw128(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes, 1024);
+                        tc_mma_pair<T::kKind>(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(empty0 + 8 * stage, 0x3);   // frees the slot in both CTAs
+                    if (++stage == kPStages) stage = 0, phase ^= 1u;
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(accf0 + 8 * buf, 0x3);          // both epilogues may read
+            }
+            tc_commit_pair(drain_bar);
+            if (!drain_wait(drain_bar, 0, limit_ns)) atomicOr(err, kErrTimeout);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        const uint32_t acce_leader0 = mapa_shared(acce0, 0);
+        int stored = 0;   // TMA stores issued by this warp (lane 0's count, shared)
+        int lt = 0;
+        for (int p = cluster_id; p < npairs; p += nclusters, ++lt) {
+            int m0, n0;
+            coords(p, m0, n0);
+            const int buf = lt & 1;
+            const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(accf0 + 8 * buf, use_parity, abort_flag, err, limit_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int row0 = m0 + (int)rank * kBM + quarter * 32;   // this warp's 32 rows
+            const int row = row0 + lane;
+            float* crow = C + (int64_t)row * N;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
+#pragma unroll 1
+            for (int c = 0; c < kAccCols / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
+                tmem_ld_wait();
+                const int col0 = n0 + c * 32;
+                if (c_mode == kStoreTma) {
+                    // Stage the warp's 32 x 32 block (row = lane) with the 128-byte
+                    // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then
+                    // one lane writes it with a TMA store that clips at M and N.
+                    const uint32_t stg = sC + (uint32_t)((quarter * 2 + (stored & 1)) * 4096);
+                    if (stored >= 2) {
+                        if (lane == 0) bulk_wait_group_read<1>();   // this buffer's last store has read it
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), v[4 * j],
+                                     v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0 && row0 < M && col0 < N) {
+                        tma_store_2d(&map_c, stg, col0, row0);
+                        bulk_commit_group();
+                        ++stored;
+                    }
+                    stored = __shfl_sync(0xffffffffu, stored, 0);
+                } else if (row < M) {
+                    if (c_mode == kStoreVec && col0 + 32 <= N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(crow + col0 + j) =
+                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce_leader0 + 8 * buf);
+        }
+        if (lane == 0) bulk_wait_group<0>();   // every store of this warp has completed
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no more signals or MMAs between the two CTAs after this
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
 }  // namespace
 
 TcShape tc_shape(TcMode mode) {
@@ -289,12 +555,88 @@ static cudaError_t set_attr() {
                                 (int)kSmemBytes);
 }
 
+template <TcMode MODE, bool BK>
+static cudaError_t set_pair_attr() {
+    return cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE, BK>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+}
+
+// Clusters of two that can be resident at once (0: pairs unavailable).
+static int g_max_pairs = 0;
+
+template <TcMode MODE, bool BK>
+static int query_max_pairs(int num_sms) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<MODE, BK>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 cudaError_t tc_setup() {
     cudaError_t e;
     if ((e = set_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
     if ((e = set_attr<TcMode::kBF16, true>()) != cudaSuccess) return e;
     if ((e = set_attr<TcMode::kTF32, false>()) != cudaSuccess) return e;
-    return set_attr<TcMode::kTF32, true>();
+    if ((e = set_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int a = query_max_pairs<TcMode::kBF16, false>(sms);
+    const int b = query_max_pairs<TcMode::kTF32, true>(sms);
+    g_max_pairs = a < b ? a : b;
+    return cudaSuccess;
+}
+
+int tc_max_pairs() { return g_max_pairs; }
+
+cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+                                const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
+                                int N, int K, bool c_vec, unsigned* err, uint64_t limit_ns,
+                                cudaStream_t stream) {
+    const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
+    const int64_t pairs = (int64_t)pairs_m * tiles_n;
+    if (pairs <= 0) return cudaSuccess;
+    if (pairs > 0x3FFFFFFF || g_max_pairs <= 0) return cudaErrorInvalidValue;
+    const int clusters = (int)(pairs < g_max_pairs ? pairs : g_max_pairs);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const int cm = map_c ? kStoreTma : (c_vec ? kStoreVec : kStoreScalar);
+    const CUtensorMap& mc = map_c ? *map_c : map_a;   // unused unless cm == kStoreTma
+    cudaError_t e;
+    if (mode == TcMode::kBF16 && !b_k_major)
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, C,
+                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+    else if (mode == TcMode::kTF32 && b_k_major)
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, C,
+                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+    else
+        return cudaErrorInvalidValue;
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
