@@ -49,6 +49,44 @@ __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst,
     }
 }
 
+// Vector form for 32-bit elements when B's rows are 16-byte aligned
+// (cols % 4 == 0, 16-byte aligned base) and dst_ld % 4 == 0: 64 x 64 tiles,
+// every global access 16 bytes wide, 4 loads in flight per thread.  Rows
+// beyond `rows` read as zero; dst columns up to roundup(rows, 4) are written
+// (the padding is inside dst's row stride and is never read as data).
+__global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restrict__ src,
+                                                           float* __restrict__ dst, int64_t rows,
+                                                           int64_t cols, int64_t dst_ld) {
+    __shared__ float tile[64][65];
+    const int t = threadIdx.x;
+    const int64_t c0 = (int64_t)blockIdx.x * 64;   // src column = dst row
+    const int64_t cols4 = cols / 4;
+    for (int64_t r0 = (int64_t)blockIdx.y * 64; r0 < rows; r0 += (int64_t)gridDim.y * 64) {
+        float4 v[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {               // src rows r0 + t/16 + 16p, columns c0 + 4(t%16)
+            const int64_t r = r0 + t / 16 + 16 * p, c4 = c0 / 4 + t % 16;
+            v[p] = (r < rows && c4 < cols4) ? src[r * cols4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int rr = t / 16 + 16 * p, cc = 4 * (t % 16);
+            tile[rr][cc] = v[p].x, tile[rr][cc + 1] = v[p].y;
+            tile[rr][cc + 2] = v[p].z, tile[rr][cc + 3] = v[p].w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {               // dst row c0 + t/16 + 16p, columns r0 + 4(t%16)
+            const int dr = t / 16 + 16 * p, dk = 4 * (t % 16);
+            const int64_t row = c0 + dr, k = r0 + dk;
+            if (row < cols && k < rows)             // k < rows: the chunk starts inside src
+                *reinterpret_cast<float4*>(dst + row * dst_ld + k) =
+                    make_float4(tile[dk][dr], tile[dk + 1][dr], tile[dk + 2][dr], tile[dk + 3][dr]);
+        }
+        __syncthreads();
+    }
+}
+
 __global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
@@ -93,6 +131,15 @@ cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t co
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
                              int64_t dst_ld, int es, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (es == 4 && cols % 4 == 0 && dst_ld % 4 == 0 &&
+        (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        const int64_t vx = (cols + 63) / 64, vy = (rows + 63) / 64;
+        if (vx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        dim3 vgrid((unsigned)vx, (unsigned)(vy < 65535 ? vy : 65535));
+        transpose_v4_kernel<<<vgrid, 256, 0, stream>>>(static_cast<const float4*>(src),
+                                                       static_cast<float*>(dst), rows, cols, dst_ld);
+        return cudaGetLastError();
+    }
     const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535)), block(32, 8);
