@@ -3,26 +3,30 @@
 // C_ij = sum_k A_ik B_kj ("Shared Memory Tiling for Matrix Multiplication",
 // opening formula), row-major as in "Matrix Multiplication -- Naive to
 // Tiled", section 02.  Every C_ij is one chain of fused multiply-adds with k
-// ascending, so the result is the sequential binary32 sum of exact products.
+// ascending, so the result is the sequential binary32 sum of exact products
+// (for the tiles of a partial last wave: the sum, in order, of such chains
+// over consecutive K ranges).
 //
 // Design (GB300 rather than the pages' 16x16/32x32 tiles):
-//   * A CTA of 256 threads owns a 128 x 128 tile of C; a thread owns an 8 x 8
-//     register block, laid out as 2 x 2 sub-blocks of 4 x 4 so each fragment
-//     is one 128-bit shared-memory load.  Per k a thread does 64 FMAs for 4
-//     fragment loads -- the register blocking of "From 306 ms to 86 ms"
-//     (4 x 4 there) and "Further Optimisation Ideas" of the first page,
-//     taken to 8 x 8.
-//   * K is walked in slabs of 16 through a 4-stage ring of shared-memory
+//   * A CTA owns a 128 x 128 tile of C and each thread a TM x TN register
+//     block, made of 4 x 4 sub-blocks so that every fragment is one 128-bit
+//     shared-memory load -- the register blocking of "From 306 ms to 86 ms"
+//     (4 x 4 there) and of "Further Optimisation Ideas" on the first page,
+//     taken further.  The lanes of a warp are laid out so that each
+//     quarter-warp reads at most two distinct 16-byte chunks of one operand:
+//     such a 128-bit load costs two shared-memory wavefronts instead of four.
+//   * K is walked in slabs of 16 through a multi-stage ring of shared-memory
 //     buffers filled by cp.async, so global loads of later slabs overlap the
 //     arithmetic on the current one (the page's "double buffering", deeper).
 //   * The A slab is stored transposed (k-major, [k][m], padded by 4 floats) so
-//     that a thread's 4 consecutive rows of A at one k are one 128-bit load;
-//     the element-wise cp.async that does the transposition is arranged so a
-//     warp's 32 stores hit 32 different banks.  B slabs are copied 16 bytes
-//     at a time when rows are 16-byte aligned, else 4 bytes at a time.
-//   * Out-of-range elements of the last slabs are zero-filled by the copy
-//     (source size 0) and out-of-range C elements are never stored -- the
-//     boundary handling of the first page's section 05, for any M, K, N.
+//     that 4 consecutive rows of A at one k are one 128-bit load; the
+//     element-wise copies that do the transposition are arranged so a warp's
+//     32 stores hit 32 different banks.  B slabs are copied 16 bytes at a time
+//     when rows are 16-byte aligned, else 4 bytes at a time.
+//   * Tiles wholly inside M and N copy their slabs without any check; edge
+//     tiles and the last, partial slab zero-fill out-of-range elements
+//     (source size 0) and store only in-range C elements -- the boundary
+//     handling of the first page's section 05, for any M, K, N.
 //   * Tiles are visited in groups of 8 tile-rows so CTAs running together
 //     share A and B slabs in L2.
 #include "kernels.h"
@@ -32,49 +36,62 @@ namespace libgemm {
 namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 16;
-constexpr int kWM = 64, kWN = 32;               // warp tile
-constexpr int kStages = 4;
-constexpr int kMinBlocks = 2;                   // CTAs per SM the register budget allows
-constexpr int kThreads = (kBM / kWM) * (kBN / kWN) * 32;  // 256
-constexpr int kLM = kWM / 8, kLN = kWN / 8;     // lanes along m / n: 8 x 4
 constexpr int kPadA = 4;
 constexpr int kLdA = kBM + kPadA;               // floats per k-row of the A slab
 constexpr int kLdB = kBN;
 constexpr int kAStage = kBK * kLdA;             // floats
 constexpr int kBStage = kBK * kLdB;
-constexpr size_t kSmemBytes = size_t(kStages) * (kAStage + kBStage) * sizeof(float);
 constexpr int kGroupM = 8;
 
-static_assert(kLM * kLN == 32, "a warp is 32 lanes");
-static_assert(kThreads == 256, "launch shape");
-static_assert((kBM * kBK) % kThreads == 0 && (kBK * kBN) % (4 * kThreads) == 0, "load split");
+// A thread-tile layout.  LM x LN lanes per warp, each lane TM x TN outputs
+// (TM/4 row chunks LM*4 apart, TN/4 column chunks LN*4 apart); kNMajor puts
+// consecutive lanes along N (ln = lane % LN) instead of along M.
+template <int TM_, int TN_, int LM_, int LN_, bool kNMajor_, int THREADS_, int STAGES_, int MINB_>
+struct Cfg {
+    static constexpr int TM = TM_, TN = TN_, LM = LM_, LN = LN_;
+    static constexpr bool kNMajor = kNMajor_;
+    static constexpr int kThreads = THREADS_, kStages = STAGES_, kMinBlocks = MINB_;
+    static constexpr int WM = LM * TM, WN = LN * TN;             // warp tile
+    static constexpr int kWarpsM = kBM / WM, kWarpsN = kBN / WN;
+    static constexpr size_t kSmemBytes = size_t(kStages) * (kAStage + kBStage) * sizeof(float);
+    static_assert(LM * LN == 32, "a warp is 32 lanes");
+    static_assert(kWarpsM * kWarpsN * 32 == kThreads, "warps cover the tile");
+    static_assert(TM % 4 == 0 && TN % 4 == 0, "4 x 4 sub-blocks");
+};
+// 8 x 8 per thread, 256 threads, lanes 8 (M) x 4 (N).
+using Cfg8x8 = Cfg<8, 8, 8, 4, false, 256, 4, 2>;
+// 16 x 8 per thread, 128 threads, lanes 4 (M) x 8 (N) with N fastest: a
+// quarter-warp shares one A chunk, so 6 fragment loads per k cost 16
+// wavefronts for 128 FMAs (the 8 x 8 layout: 12 for 64).
+using Cfg16x8 = Cfg<16, 8, 4, 8, true, 128, 3, 3>;
+using FfmaCfg = Cfg16x8;
 
 // The copies of one thread, planned once per tile so that issuing the copies
-// of a K slab is a few pointer and address additions.  Slabs that lie wholly
-// inside K need no K check; only the last one, when K % kBK != 0, has it.
+// of a K slab is a few pointer and address additions.
 //
 // A: kBM x kBK elements, kAPer per thread.  A pass covers 8 consecutive k of
-// kThreads/8 rows; lanes 0-7 take one row, so a warp reads 4 x 32 contiguous
+// THREADS/8 rows; lanes 0-7 take one row, so a warp reads 4 x 32 contiguous
 // bytes and its transposed stores land in banks (4*k + row) mod 32, all
 // distinct.  B: rows of kBN columns copied 16 bytes (kBVec) or 4 bytes per
 // copy, a warp covering one contiguous 512- or 128-byte row piece.
-template <bool kBVec>
+template <bool kBVec, int THREADS>
 struct SlabLoader {
-    static constexpr int kRowsPerPass = kThreads / 8;              // 32 rows of A per pass
-    static constexpr int kARowGroups = kBM / kRowsPerPass;         // 4
-    static constexpr int kAPer = (kBM * kBK) / kThreads;           // 8 copies of A
+    static constexpr int kRowsPerPass = THREADS / 8;               // rows of A per pass
+    static constexpr int kARowGroups = kBM / kRowsPerPass;
+    static constexpr int kAPer = (kBM * kBK) / THREADS;            // copies of A per thread
     static constexpr int kBElems = kBVec ? 4 : 1;                  // floats per B copy
     static constexpr int kBPerRow = kBN / kBElems;                 // copies per B row
-    static constexpr int kBRowsPerPass = kThreads / kBPerRow;      // 8 (vec) or 2
-    static constexpr int kBPer = kBK / kBRowsPerPass;              // 2 (vec) or 8
-    static_assert(kThreads % kBPerRow == 0 && kBK % kBRowsPerPass == 0, "B split");
+    static constexpr int kBRowsPerPass = THREADS / kBPerRow;
+    static constexpr int kBPer = kBK / kBRowsPerPass;              // copies of B per thread
+    static_assert(kAPer == kARowGroups * (kBK / 8), "A split");
+    static_assert(THREADS % kBPerRow == 0 && kBK % kBRowsPerPass == 0, "B split");
 
     const float* a_base;               // A itself: source of zero-size copies
     const float* a_ptr;                // &A[m0 + tid/8][tid % 8]
     const float* b_ptr;                // &B[tid / kBPerRow][n0 + column of this thread]
     int64_t a_group_step;              // kRowsPerPass * K: to the next row group of A
     int64_t n;                         // N, the row stride of B
-    uint32_t a_row_ok;                 // bit j: row of a_row[j] < M
+    uint32_t a_row_ok;                 // bit j: row group j of this thread is < M
     bool b_col_ok;
     int a_k, b_k;                      // this thread's k offset within a slab (A, B)
     uint32_t a_dst, b_dst;             // shared addresses in ring slot 0
@@ -109,7 +126,7 @@ struct SlabLoader {
         for (int j = 0; j < kARowGroups; ++j) {
             const float* row = a_ptr + j * a_group_step + k0;
 #pragma unroll
-            for (int g = 0; g < kAPer / kARowGroups; ++g)
+            for (int g = 0; g < kBK / 8; ++g)
                 cp_async_4(adst + (uint32_t)((8 * g * kLdA + kRowsPerPass * j) * 4), row + 8 * g);
         }
         const uint32_t bdst = b_dst + (uint32_t)(slot * kBStage * 4);
@@ -162,12 +179,13 @@ struct SlabLoader {
 // such CTA writes its partial tile to `partial`, and the last of them to
 // finish (an atomic counter per tile) adds the partials in split order and
 // stores C.  The sum is then ((p0 + p1) + p2) + ..., the same on every run.
-template <bool kBVec, bool kCVec>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
+template <class CF, bool kBVec, bool kCVec>
+__global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     ffma_sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                       float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
                       int dp_tiles, int splits, float* __restrict__ partial,
                       unsigned* __restrict__ counters) {
+    constexpr int TM = CF::TM, TN = CF::TN, kStages = CF::kStages;
     extern __shared__ __align__(16) float smem[];
     float* sA = smem;                          // kStages x [kBK][kLdA]
     float* sB = smem + kStages * kAStage;      // kStages x [kBK][kLdB]
@@ -196,22 +214,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm0 = (warp / (kBN / kWN)) * kWM;
-    const int wn0 = (warp % (kBN / kWN)) * kWN;
-    const int lm = lane % kLM, ln = lane / kLM;
-    const int am = wm0 + lm * 4;               // rows am..am+3 and am+kWM/2..+3
-    const int bn = wn0 + ln * 4;               // cols bn..bn+3 and bn+kWN/2..+3
+    const int wm0 = (warp / CF::kWarpsN) * CF::WM;
+    const int wn0 = (warp % CF::kWarpsN) * CF::WN;
+    const int lm = CF::kNMajor ? lane / CF::LN : lane % CF::LM;
+    const int ln = CF::kNMajor ? lane % CF::LN : lane / CF::LM;
+    const int am = wm0 + lm * 4;               // row chunks am + c*LM*4, c < TM/4
+    const int bn = wn0 + ln * 4;               // column chunks bn + c*LN*4, c < TN/4
+    // row / column (in the tile) of the i-th / j-th element of this thread's block
+    auto row_of = [&](int i) { return am + (i / 4) * (CF::LM * 4) + (i % 4); };
+    auto col_of = [&](int j) { return bn + (j / 4) * (CF::LN * 4) + (j % 4); };
 
-    float acc[8][8];
+    // Accumulators in pairs of rows: acc2[p][j] = (C[2p][j], C[2p+1][j]) of this
+    // thread's block, updated with packed two-lane FMAs (each lane one
+    // round-to-nearest FMA, exactly as the scalar instruction).
+    float2 acc2[TM / 2][TN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int p = 0; p < TM / 2; ++p)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc2[p][j] = make_float2(0.0f, 0.0f);
+    auto acc = [&](int i, int j) -> float& { return (i & 1) ? acc2[i >> 1][j].y : acc2[i >> 1][j].x; };
 
-    const SlabLoader<kBVec> loader(A, B, sA, sB, M, N, K, m0, n0, tid);
+    const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, m0, n0, tid);
     const int full_slabs = K / kBK;   // slabs kt < full_slabs lie wholly inside K
     const int nloc = kt_end - kt_begin;
-
     // Slabs before interior_end can take the unchecked copies.
     const bool interior = m0 + kBM <= M && n0 + kBN <= N;
     const int interior_end = interior ? full_slabs : 0;
@@ -242,16 +267,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         const float* b_s = sB + (i % kStages) * kBStage;
 #pragma unroll
         for (int k = 0; k < kBK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4*>(a_s + k * kLdA + am);
-            const float4 a1 = *reinterpret_cast<const float4*>(a_s + k * kLdA + am + kWM / 2);
-            const float4 b0 = *reinterpret_cast<const float4*>(b_s + k * kLdB + bn);
-            const float4 b1 = *reinterpret_cast<const float4*>(b_s + k * kLdB + bn + kWN / 2);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float2 a2[TM / 2];
+            float b[TN];
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii)
+            for (int c = 0; c < TM / 4; ++c) {
+                const float4 t = *reinterpret_cast<const float4*>(a_s + k * kLdA + am + c * CF::LM * 4);
+                a2[2 * c] = make_float2(t.x, t.y), a2[2 * c + 1] = make_float2(t.z, t.w);
+            }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[ii][j] = fmaf(a[ii], b[j], acc[ii][j]);
+            for (int c = 0; c < TN / 4; ++c) {
+                const float4 t = *reinterpret_cast<const float4*>(b_s + k * kLdB + bn + c * CF::LN * 4);
+                b[4 * c] = t.x, b[4 * c + 1] = t.y, b[4 * c + 2] = t.z, b[4 * c + 3] = t.w;
+            }
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const float2 bj = make_float2(b[j], b[j]);
+#pragma unroll
+                for (int pp = 0; pp < TM / 2; ++pp) acc2[pp][j] = __ffma2_rn(a2[pp], bj, acc2[pp][j]);
+            }
         }
     }
     cp_async_wait<0>();
@@ -262,13 +295,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         const int st = tile - dp_tiles;
         float* mine = partial + ((int64_t)st * splits + part) * (kBM * kBN);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = am + (i < 4 ? i : kWM / 2 + (i - 4));
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                *reinterpret_cast<float4*>(mine + r * kBN + bn + h * (kWN / 2)) =
-                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
-        }
+            for (int h = 0; h < TN / 4; ++h)
+                *reinterpret_cast<float4*>(mine + row_of(i) * kBN + col_of(4 * h)) =
+                    make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2), acc(i, 4 * h + 3));
         __threadfence();
         __syncthreads();
         if (tid == 0) s_last = atomicAdd(counters + st, 1u) == (unsigned)(splits - 1);
@@ -277,39 +308,38 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         __threadfence();
         const float* base = partial + (int64_t)st * splits * (kBM * kBN);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = am + (i < 4 ? i : kWM / 2 + (i - 4));
+        for (int i = 0; i < TM; ++i) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = r * kBN + bn + h * (kWN / 2);
+            for (int h = 0; h < TN / 4; ++h) {
+                const int c = row_of(i) * kBN + col_of(4 * h);
                 float4 sum = __ldcg(reinterpret_cast<const float4*>(base + c));
                 for (int p = 1; p < splits; ++p) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)p * (kBM * kBN) + c));
                     sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
                 }
-                acc[i][4 * h] = sum.x, acc[i][4 * h + 1] = sum.y;
-                acc[i][4 * h + 2] = sum.z, acc[i][4 * h + 3] = sum.w;
+                acc(i, 4 * h) = sum.x, acc(i, 4 * h + 1) = sum.y;
+                acc(i, 4 * h + 2) = sum.z, acc(i, 4 * h + 3) = sum.w;
             }
         }
     }
 
-    // Store the 8 x 8 block: guarded against M and N.
+    // Store the block: guarded against M and N.
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + am + (i < 4 ? i : kWM / 2 + (i - 4));
+    for (int i = 0; i < TM; ++i) {
+        const int row = m0 + row_of(i);
         if (row >= M) continue;
         float* crow = C + (int64_t)row * N;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int col = n0 + bn + h * (kWN / 2);
+        for (int h = 0; h < TN / 4; ++h) {
+            const int col = n0 + col_of(4 * h);
             if (kCVec && col < N) {   // N % 4 == 0: all four columns are in range
                 *reinterpret_cast<float4*>(crow + col) =
-                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
-                                acc[i][4 * h + 3]);
+                    make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2),
+                                acc(i, 4 * h + 3));
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (col + j < N) crow[col + j] = acc[i][4 * h + j];
+                    if (col + j < N) crow[col + j] = acc(i, 4 * h + j);
             }
         }
     }
@@ -317,11 +347,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 
 template <bool BV, bool CV>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<BV, CV>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)FfmaCfg::kSmemBytes);
 }
 
-int g_ctas_per_sm = kMinBlocks;
+int g_ctas_per_sm = FfmaCfg::kMinBlocks;
 
 }  // namespace
 
@@ -332,8 +363,8 @@ cudaError_t ffma_setup() {
     if ((e = set_smem_attr<true, false>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<true, true>()) != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffma_sgemm_kernel<true, true>, kThreads,
-                                                      kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffma_sgemm_kernel<FfmaCfg, true, true>,
+                                                      FfmaCfg::kThreads, FfmaCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     g_ctas_per_sm = n > 0 ? n : 1;
     return cudaSuccess;
@@ -374,12 +405,12 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
     if (plan.tiles <= 0) return cudaSuccess;
     const int64_t ctas = plan.dp_tiles + plan.split_tiles * plan.splits;
     if (ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    dim3 grid((unsigned)ctas), block(kThreads);
+    dim3 grid((unsigned)ctas), block(FfmaCfg::kThreads);
     const int dp = (int)plan.dp_tiles, sp = plan.splits;
-#define LIBGEMM_FFMA_LAUNCH(BV, CV)                                                               \
-    ffma_sgemm_kernel<BV, CV><<<grid, block, kSmemBytes, stream>>>(A, B, C, M, N, K, tiles_m,     \
-                                                                    tiles_n, dp, sp, partial,     \
-                                                                    counters)
+    const size_t smem = FfmaCfg::kSmemBytes;
+#define LIBGEMM_FFMA_LAUNCH(BV, CV)                                                            \
+    ffma_sgemm_kernel<FfmaCfg, BV, CV><<<grid, block, smem, stream>>>(                         \
+        A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters)
     if (b_vec && c_vec) LIBGEMM_FFMA_LAUNCH(true, true);
     else if (b_vec) LIBGEMM_FFMA_LAUNCH(true, false);
     else if (c_vec) LIBGEMM_FFMA_LAUNCH(false, true);
