@@ -61,6 +61,8 @@ def _load():
             lib.oracle_sum.argtypes = [ip, vp, vp, i64, i64, i64, dp, dp]
             lib.oracle_widen.argtypes = [ip, vp, i64, dp]
             lib.oracle_threads.argtypes = [ip]
+            lib.oracle_gemm_f32_chain.argtypes = [vp, vp, i64, i64, i64, vp, ip]
+            lib.oracle_gemm_f32_chain.restype = ctypes.c_int
             for f in (lib.oracle_gemm, lib.oracle_dot, lib.oracle_sum,
                       lib.oracle_widen, lib.oracle_threads):
                 f.restype = ctypes.c_int
@@ -106,6 +108,16 @@ def gemm(A: np.ndarray, B: np.ndarray, fmt: str = "f32", nthreads: int = 0):
     if rc != 0:
         raise RuntimeError("oracle_gemm failed")
     return C, S
+
+
+def fma_chain(A: np.ndarray, B: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """float32 C with C_ij = the binary32 chain acc = fma(A_ik, B_kj, acc), k ascending."""
+    A, B = _as_input(A, "f32"), _as_input(B, "f32")
+    M, K, N = _dims(A, B)
+    C = np.empty((M, N), np.float32)
+    if _load().oracle_gemm_f32_chain(_ptr(A), _ptr(B), M, K, N, _ptr(C), int(nthreads)) != 0:
+        raise RuntimeError("oracle_gemm_f32_chain failed")
+    return C
 
 
 def dot(A: np.ndarray, B: np.ndarray, rows, cols, fmt: str = "f32", nthreads: int = 0):

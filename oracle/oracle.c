@@ -35,6 +35,13 @@
  * library is built with -ffp-contract=off so that x86 and Arm agree bit for
  * bit.
  *
+ * oracle_gemm_f32_chain is a second, narrower reference: the product as a
+ * binary32 machine computes it with one fused multiply-add per term, k
+ * ascending (fmaf is correctly rounded in C99).  The pages leave the order
+ * and rounding of the sum open; this is the reading the library's FP32 mode
+ * documents, and tests compare it bit for bit where the library does not split
+ * the K range.
+ *
  * Parity pins (tests/test_oracle.py): identity and permutation matrices,
  * hand-worked integer products (tests/golden/), rank-1 closed forms, all-ones
  * inputs, the sum identity, S against C on non-negative inputs, the exact
@@ -206,6 +213,27 @@ int oracle_sum(int fmt, const void* A, const void* B, int64_t M, int64_t K,
     }
     *total = t;
     if (abs_total) *abs_total = ta;
+    return 0;
+}
+
+/*
+ * C[i*N+j] = the binary32 chain acc = fmaf(A_ik, B_kj, acc), k = 0 .. K-1,
+ * from acc = 0.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemm_f32_chain(const float* A, const float* B, int64_t M, int64_t K, int64_t N,
+                          float* C, int nthreads) {
+    if (M < 0 || K < 0 || N < 0 || (M > 0 && K > 0 && !A) || (K > 0 && N > 0 && !B) ||
+        (M > 0 && N > 0 && !C))
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc = fmaf(A[i * K + k], B[k * N + j], acc);
+            C[i * N + j] = acc;
+        }
+    }
     return 0;
 }
 

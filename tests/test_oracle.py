@@ -208,3 +208,47 @@ def test_rejects_bad_arguments():
         oracle.gemm(A, np.ones((3, 2), np.float64))
     with pytest.raises(ValueError):
         oracle.gemm(A, np.ones((3, 2), np.float32), fmt="fp8")
+
+
+def _chain_cases():
+    import os
+    from golden_io import GOLDEN
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "f32_chain.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "case":
+                cur = {"name": vals[0]}
+                cases.append(cur)
+            else:
+                cur[key] = np.asarray([float(v) for v in vals])
+    return cases
+
+
+@pytest.mark.parametrize("case", _chain_cases(), ids=lambda c: c["name"])
+def test_f32_chain_hand_cases(case):
+    A = case["A"].astype(np.float32).reshape(1, -1)
+    B = case["B"].astype(np.float32).reshape(-1, 1)
+    assert A.astype(np.float64).tolist()[0] == case["A"].tolist()      # exact in binary32
+    C = oracle.fma_chain(A, B)
+    assert float(C[0, 0]) == float(case["C"][0])
+
+
+def test_f32_chain_exact_on_integers():
+    A, B = inputs.matrices(23, 200, 17, "int4", seed=13)
+    C = oracle.fma_chain(A, B)
+    ref, _ = oracle.gemm(A, B)
+    np.testing.assert_array_equal(C.astype(np.float64), ref)
+
+
+def test_f32_chain_within_binary32_bound():
+    A, B = inputs.matrices(31, 300, 29, "pm1", seed=14)
+    C = oracle.fma_chain(A, B).astype(np.float64)
+    ref, S = oracle.gemm(A, B)
+    u = 2.0 ** -24
+    g = 300 * u / (1 - 300 * u)
+    assert np.all(np.abs(C - ref) <= g * S)
+    assert np.any(C != ref)            # it really is binary32 arithmetic

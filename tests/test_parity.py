@@ -93,3 +93,23 @@ def test_sweep_large_sampled(libgemm, mode, n):
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
 def test_large_8192_sampled(libgemm, mode):
     _sampled_case(libgemm, 8192, 8192, 8192, "pm1", mode)
+
+
+@pytest.mark.parametrize("M,K,N", [(1000, 240, 1500), (257, 129, 383), (128, 16, 128),
+                                   (4096, 64, 4096), (3, 1, 5)])
+def test_fp32_is_the_binary32_fma_chain(libgemm, M, K, N):
+    """FP32 mode, bit for bit: each C_ij is acc = fma(A_ik, B_kj, acc), k
+    ascending.  (K <= 240 is 15 slabs of 16, too few for the library to
+    split a tile's K range.)"""
+    A, B = inputs.matrices(M, K, N, "pm1", seed=M + 7 * K + 13 * N)
+    C = run(libgemm, A, B, "fp32")
+    np.testing.assert_array_equal(C, oracle.fma_chain(A, B))
+
+
+def test_fp32_fma_chain_hand_cases(libgemm):
+    from test_oracle import _chain_cases
+    for case in _chain_cases():
+        A = case["A"].astype(np.float32).reshape(1, -1)
+        B = case["B"].astype(np.float32).reshape(-1, 1)
+        C = run(libgemm, A, B, "fp32")
+        assert float(C[0, 0]) == float(case["C"][0]), case["name"]
