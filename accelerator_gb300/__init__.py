@@ -6,9 +6,9 @@ loads nothing: the library is opened at the first call, and a missing library
 is an error, never a fallback.
 """
 
-FP32, TF32, BF16 = 0, 1, 2
+FP32, TF32, BF16, FP16 = 0, 1, 2, 3
 
-__all__ = ["gemm", "GemmError", "FP32", "TF32", "BF16"]
+__all__ = ["gemm", "GemmError", "FP32", "TF32", "BF16", "FP16"]
 
 
 def __getattr__(name):

@@ -12,8 +12,8 @@ import threading
 
 from . import build as _build
 
-FP32, TF32, BF16 = 0, 1, 2
-MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16}
+FP32, TF32, BF16, FP16 = 0, 1, 2, 3
+MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16, "fp16": FP16}
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -86,15 +86,15 @@ def _stream_ptr(stream) -> int:
 def gemm(A, B, C=None, mode=FP32, stream=None):
     """C = A @ B on the current CUDA device with libgemm.
 
-    A (M x K) and B (K x N): contiguous CUDA tensors, float32 for FP32/TF32 or
-    bfloat16 for BF16.  C: a contiguous float32 (M x N) CUDA tensor to
+    A (M x K) and B (K x N): contiguous CUDA tensors, float32 for FP32/TF32,
+    bfloat16 for BF16, float16 for FP16.  C: a contiguous float32 (M x N) CUDA tensor to
     overwrite, or None to allocate one.  Returns C.  Asynchronous on `stream`
     (default: torch's current stream).
     """
     import torch
     if isinstance(mode, str):
         mode = MODES[mode.lower()]
-    want = torch.bfloat16 if mode == BF16 else torch.float32
+    want = {BF16: torch.bfloat16, FP16: torch.float16}.get(mode, torch.float32)
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shapes {tuple(A.shape)} and {tuple(B.shape)} do not chain")
     for name, t in (("A", A), ("B", B)):

@@ -97,9 +97,7 @@ bool ranges_overlap(uintptr_t a, uint64_t abytes, uintptr_t b, uint64_t bbytes) 
 // 2-D tensor map over a rows x cols row-major matrix with row stride ld
 // (elements), box box_cols x box_rows, 128-byte swizzle, zero fill outside.
 int encode_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols, int64_t ld,
-              int box_cols, int box_rows) {
-    const CUtensorMapDataType dt =
-        es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+              int box_cols, int box_rows, CUtensorMapDataType dt) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
@@ -145,9 +143,16 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
     return rc;
 }
 
+CUtensorMapDataType tensor_type(TcMode mode) {
+    return mode == TcMode::kTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+           : mode == TcMode::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
 int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
                      int64_t N, DeviceState* st, cudaStream_t stream) {
-    const int es = mode == TcMode::kBF16 ? 2 : 4;
+    const int es = mode == TcMode::kTF32 ? 4 : 2;
+    const CUtensorMapDataType dt = tensor_type(mode);
     const TcShape shape = tc_shape(mode);
     const int64_t align_elems = 16 / es;
     // BF16 reads B as an MN-major operand, straight from the caller's K x N
@@ -197,15 +202,15 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
     const bool pairs = tc_max_pairs() > 0;
     const int b_rows = pairs ? shape.block_n / 2 : shape.block_n;
     CUtensorMap map_a, map_b;
-    int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m);
+    int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m, dt);
     if (rc == GEMM_OK)
-        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows)
-                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems);
+        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows, dt)
+                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt);
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
     // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
     CUtensorMap map_c;
     const bool c_tma = pairs && c_vec && rc == GEMM_OK &&
-                       encode_2d(&map_c, C, 4, M, N, N, 32, 32) == GEMM_OK;
+                       encode_2d(&map_c, C, 4, M, N, N, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) == GEMM_OK;
     if (rc == GEMM_OK) {
         const cudaError_t e =
             pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
@@ -238,7 +243,8 @@ int device_setup(int* num_sms, unsigned** err) {
 
 int encode_tensor_map_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols,
                          int64_t ld, int box_cols, int box_rows) {
-    return encode_2d(map, ptr, es, rows, cols, ld, box_cols, box_rows);
+    return encode_2d(map, ptr, es, rows, cols, ld, box_cols, box_rows,
+                     es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
 void count_launch() { g_launches++; }
@@ -250,13 +256,14 @@ extern "C" {
 int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
          int precision_mode, struct CUstream_st* stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16)
+    if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16 &&
+        precision_mode != GEMM_FP16)
         return GEMM_ERR_INVALID_ARG;
     if (M < 0 || K < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
     // Every dimension must fit the kernels' 32-bit indices and TMA coordinates.
     const int64_t kDimMax = 0x7FFFFFFF;
     if (M > kDimMax || K > kDimMax || N > kDimMax) return GEMM_ERR_INVALID_ARG;
-    const int es = precision_mode == GEMM_BF16 ? 2 : 4;
+    const int es = (precision_mode == GEMM_BF16 || precision_mode == GEMM_FP16) ? 2 : 4;
     const int64_t kElemMax = INT64_MAX / 16;
     if ((K && M > kElemMax / K) || (N && K > kElemMax / N) || (N && M > kElemMax / N))
         return GEMM_ERR_INVALID_ARG;
@@ -282,8 +289,10 @@ int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N
     if (precision_mode == GEMM_FP32) return ffma_gemm(static_cast<const float*>(A),
                                                       static_cast<const float*>(B), C, M, K, N, st,
                                                       stream);
-    return tensor_core_gemm(precision_mode == GEMM_BF16 ? TcMode::kBF16 : TcMode::kTF32, A, B, C,
-                            M, K, N, st, stream);
+    const TcMode tm = precision_mode == GEMM_BF16   ? TcMode::kBF16
+                      : precision_mode == GEMM_FP16 ? TcMode::kF16
+                                                    : TcMode::kTF32;
+    return tensor_core_gemm(tm, A, B, C, M, K, N, st, stream);
 }
 
 const char* gemm_status_string(int status) {

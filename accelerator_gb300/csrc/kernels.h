@@ -26,7 +26,7 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
                               unsigned* counters, cudaStream_t stream);
 
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
-enum class TcMode { kBF16, kTF32 };
+enum class TcMode { kBF16, kTF32, kF16 };
 struct TcShape {
     int block_m, block_n;   // output tile per CTA
     int k_elems;            // K elements per pipeline stage (128 bytes)

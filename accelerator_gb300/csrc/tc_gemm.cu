@@ -62,6 +62,12 @@ struct Traits<TcMode::kBF16> {
     static constexpr TcKind kKind = TcKind::kF16;
 };
 template <>
+struct Traits<TcMode::kF16> {
+    static constexpr int kEs = 2;
+    static constexpr uint32_t kFormat = 0;       // F16
+    static constexpr TcKind kKind = TcKind::kF16;
+};
+template <>
 struct Traits<TcMode::kTF32> {
     static constexpr int kEs = 4;
     static constexpr uint32_t kFormat = 2;       // TF32
@@ -545,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 TcShape tc_shape(TcMode mode) {
-    const int es = mode == TcMode::kBF16 ? 2 : 4;
+    const int es = mode == TcMode::kTF32 ? 4 : 2;
     return TcShape{kBM, kBN, kSlabBytes / es, kSlabBytes / es};
 }
 
@@ -591,7 +597,9 @@ cudaError_t tc_setup() {
     if ((e = set_attr<TcMode::kBF16, true>()) != cudaSuccess) return e;
     if ((e = set_attr<TcMode::kTF32, false>()) != cudaSuccess) return e;
     if ((e = set_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kF16, false>()) != cudaSuccess) return e;
     if ((e = set_pair_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kF16, false>()) != cudaSuccess) return e;
     if ((e = set_pair_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -634,6 +642,9 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     else if (mode == TcMode::kTF32 && b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, C,
                                M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+    else if (mode == TcMode::kF16 && !b_k_major)
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, C,
+                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
     else
         return cudaErrorInvalidValue;
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -654,6 +665,9 @@ cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a
     if (mode == TcMode::kBF16) {
         if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kBF16, true);
         else LIBGEMM_TC_LAUNCH(TcMode::kBF16, false);
+    } else if (mode == TcMode::kF16) {
+        if (b_k_major) return cudaErrorInvalidValue;
+        LIBGEMM_TC_LAUNCH(TcMode::kF16, false);
     } else {
         if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kTF32, true);
         else LIBGEMM_TC_LAUNCH(TcMode::kTF32, false);

@@ -83,6 +83,14 @@ def sample_indices(M: int, N: int, n: int = 4096, seed: int = BASE_SEED):
     return rows, cols
 
 
+def fp16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE binary16 (numpy's conversion: to nearest,
+    ties to even); uint16 patterns.  The input recipe of the FP16-input mode:
+    the library and the oracle receive the same patterns.  Values must lie
+    within binary16's range (the workloads' do: |x| <= 4)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
 def tf32_exact(x: np.ndarray) -> np.ndarray:
     """float32 values with the low 13 fraction bits cleared, so every value is
     exactly representable in TF32 and the tensor cores read it unchanged."""

@@ -51,7 +51,12 @@ enum gemm_mode {
     /* A, B: const uint16_t* holding bfloat16 values (the caller rounds its
      * data to bfloat16).  Tensor cores (tcgen05, kind::f16 with BF16
      * inputs), binary32 accumulation. */
-    GEMM_BF16 = 2
+    GEMM_BF16 = 2,
+    /* A, B: const uint16_t* holding IEEE binary16 values.  Tensor cores
+     * (tcgen05, kind::f16 with F16 inputs), binary32 accumulation -- the
+     * FP16-input, FP32-accumulate product the first page's "Further
+     * Optimisation Ideas" names for tensor cores. */
+    GEMM_FP16 = 3
 };
 
 /* Status codes returned by every entry point (0 = success). */
@@ -61,7 +66,7 @@ enum gemm_status {
                                         dimension, unknown mode, C overlapping A or B,
                                         or a size whose element count overflows int64 */
     GEMM_ERR_MISALIGNED = 2,         /* pointer not aligned to its element size
-                                        (4 bytes for float, 2 bytes for bfloat16) */
+                                        (4 bytes for float, 2 for bfloat16/binary16) */
     GEMM_ERR_CUDA = 3,               /* a CUDA runtime call or kernel launch failed */
     GEMM_ERR_NO_MEMORY = 4,          /* the stream-ordered scratch allocation failed */
     GEMM_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 */
@@ -73,7 +78,8 @@ enum gemm_status {
 
 /*
  * C = A*B.
- *   A               device pointer to M*K elements (float, or bfloat16 in GEMM_BF16)
+ *   A               device pointer to M*K elements (float; bfloat16 in GEMM_BF16;
+ *                   binary16 in GEMM_FP16)
  *   B               device pointer to K*N elements (same element type as A)
  *   C               device pointer to M*N floats; overwritten; must not overlap A or B
  *   M, K, N         dimensions, each >= 0.  M == 0 or N == 0: nothing is done.

@@ -28,7 +28,9 @@
  *     16-bit patterns (sign, 8 exponent bits, 7 fraction bits: the top half of
  *     an IEEE binary32) and widen exactly.  The TF32 diagnostic format keeps
  *     the sign, the 8 exponent bits and the top 10 fraction bits of a binary32
- *     and clears the other 13 (truncation), then widens exactly.
+ *     and clears the other 13 (truncation), then widens exactly.  FP16 values
+ *     arrive as IEEE binary16 patterns (sign, 5 exponent bits with bias 15,
+ *     10 fraction bits; exponent 0 holds the subnormals) and widen exactly.
  *
  * Each product of two widened binary32 values has at most 48 significant
  * bits and is therefore exact in double; only the running sums round.  The
@@ -60,13 +62,22 @@ enum {
     ORACLE_F32 = 0,       /* binary32 values                          */
     ORACLE_BF16 = 1,      /* bfloat16 bit patterns (uint16)           */
     ORACLE_TF32_TRUNC = 2,/* binary32, low 13 fraction bits cleared   */
-    ORACLE_F64 = 3        /* binary64 values, used as given           */
+    ORACLE_F64 = 3,       /* binary64 values, used as given           */
+    ORACLE_F16 = 4        /* IEEE binary16 bit patterns (uint16)      */
 };
 
 static double from_bits32(uint32_t u) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* The value of an IEEE binary16 pattern (finite inputs only). */
+static double from_half(uint16_t h) {
+    const int sign = h >> 15, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+    double v = e == 0 ? ldexp((double)f, -24)                 /* subnormal: f * 2^-24 */
+                      : ldexp((double)(1024 + f), e - 25);    /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
 }
 
 /* Element idx of an input matrix in format fmt, widened exactly to double. */
@@ -81,6 +92,8 @@ static double widen(int fmt, const void* p, int64_t idx) {
         memcpy(&u, (const float*)p + idx, sizeof u);
         return from_bits32(u & 0xFFFFE000u);
     }
+    case ORACLE_F16:
+        return from_half(((const uint16_t*)p)[idx]);
     default:
         return ((const double*)p)[idx];
     }
@@ -88,7 +101,7 @@ static double widen(int fmt, const void* p, int64_t idx) {
 
 static int valid(int fmt, const void* A, const void* B, int64_t M, int64_t K,
                  int64_t N) {
-    if (fmt < ORACLE_F32 || fmt > ORACLE_F64) return 0;
+    if (fmt < ORACLE_F32 || fmt > ORACLE_F16) return 0;
     if (M < 0 || K < 0 || N < 0) return 0;
     if ((M > 0 && K > 0 && !A) || (K > 0 && N > 0 && !B)) return 0;
     return 1;
@@ -239,7 +252,7 @@ int oracle_gemm_f32_chain(const float* A, const float* B, int64_t M, int64_t K, 
 
 /* Element-wise widening of n inputs of format fmt (to test the formats). */
 int oracle_widen(int fmt, const void* p, int64_t n, double* out) {
-    if (fmt < ORACLE_F32 || fmt > ORACLE_F64 || n < 0 || (n > 0 && (!p || !out)))
+    if (fmt < ORACLE_F32 || fmt > ORACLE_F16 || n < 0 || (n > 0 && (!p || !out)))
         return -1;
     for (int64_t t = 0; t < n; ++t) out[t] = widen(fmt, p, t);
     return 0;

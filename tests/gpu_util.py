@@ -12,6 +12,9 @@ def device_operands(A: np.ndarray, B: np.ndarray, mode: str):
     if mode == "bf16":
         a = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16)
         b = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16)
+    elif mode == "fp16":
+        a = torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).view(torch.float16)
+        b = torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).view(torch.float16)
     else:
         a, b = torch.from_numpy(A), torch.from_numpy(B)
     return a.cuda(), b.cuda()
@@ -33,6 +36,8 @@ def oracle_inputs(A: np.ndarray, B: np.ndarray, mode: str):
     """(A, B, fmt) for the oracle seeing exactly the values the tensor cores see."""
     if mode == "bf16":
         return inputs.bf16_bits(A), inputs.bf16_bits(B), "bf16"
+    if mode == "fp16":
+        return inputs.fp16_bits(A), inputs.fp16_bits(B), "f16"
     if mode == "tf32":
         return A, B, "tf32"
     return A, B, "f32"

@@ -16,7 +16,7 @@ from gpu_util import device_operands, run
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["fp32", "tf32", "bf16"]
+MODES = ["fp32", "tf32", "bf16", "fp16"]
 DIMS = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257]
 
 
@@ -101,7 +101,7 @@ def test_no_writes_outside_c(libgemm, mode):
 @pytest.mark.parametrize("mode", MODES)
 def test_k_zero_is_empty_sum(libgemm, mode):
     import torch
-    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
     a = torch.empty((37, 0), dtype=dt, device="cuda")
     b = torch.empty((0, 53), dtype=dt, device="cuda")
     c = torch.full((37, 53), float("nan"), device="cuda")
@@ -113,7 +113,7 @@ def test_k_zero_is_empty_sum(libgemm, mode):
 @pytest.mark.parametrize("mode", MODES)
 def test_empty_m_or_n_is_noop(libgemm, mode):
     import torch
-    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}.get(mode, torch.float32)
     before = libgemm.launch_count()
     for (M, K, N) in [(0, 5, 7), (5, 7, 0), (0, 0, 0)]:
         a = torch.ones((M, K), dtype=dt, device="cuda")

@@ -180,6 +180,20 @@ def test_bf16_widening_known_patterns():
     assert list(got) == want
 
 
+def test_f16_widening_known_patterns():
+    bits = np.array([0x3C00, 0xC000, 0x7BFF, 0x0001, 0x0400, 0x3555, 0x8000, 0x3BFF], np.uint16)
+    want = [1.0, -2.0, 65504.0, 2.0 ** -24, 2.0 ** -14, 1365 / 4096, -0.0, 1 - 2.0 ** -11]
+    assert list(oracle.widen(bits, "f16")) == want
+
+
+def test_f16_agrees_with_numpy_half():
+    # numpy's binary16 decoding is an independent implementation of the format
+    bits = np.arange(0, 0x7C00, 7, dtype=np.uint16)          # finite, non-negative
+    bits = np.concatenate([bits, bits | 0x8000])
+    np.testing.assert_array_equal(oracle.widen(bits, "f16"),
+                                  bits.view(np.float16).astype(np.float64))
+
+
 def test_tf32_truncation_known_values():
     x = np.array([1.0, 1.0 + 2.0 ** -10, 1.0 + 2.0 ** -11, 1.0 + 2.0 ** -23,
                   -(1.0 + 2.0 ** -10 + 2.0 ** -11), 3.0, 2.0 ** -126 * (1 + 2.0 ** -12)],
@@ -195,6 +209,7 @@ def test_formats_agree_on_exact_inputs():
     A, B = inputs.matrices(9, 31, 11, "int4", seed=12)
     ref, _ = oracle.gemm(A, B, fmt="f32")
     for fmt, (a, b) in {"tf32": (A, B), "bf16": (inputs.bf16_bits(A), inputs.bf16_bits(B)),
+                        "f16": (inputs.fp16_bits(A), inputs.fp16_bits(B)),
                         "f64": (A.astype(np.float64), B.astype(np.float64))}.items():
         C, _ = oracle.gemm(a, b, fmt=fmt)
         np.testing.assert_array_equal(C, ref)

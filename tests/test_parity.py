@@ -7,6 +7,7 @@ Workloads are the seeded synthetic inputs of the pages' studies:
   * the square sweep N = 128 .. 4096 (full oracle up to 1024, then 4096+
     sampled entries and the sum-of-all-elements identity);
   * 8192^3 on the tensor-core modes, uniform on [-1, 1).
+FP16 (binary16 inputs, the tolerance of TF32) rides along in every mode list.
 Every element must satisfy |C - Cref| <= tol * S_ij; C is poisoned with NaN
 before each launch so an unwritten element fails.
 """
@@ -20,7 +21,7 @@ from gpu_util import oracle_inputs, run
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["fp32", "tf32", "bf16"]
+MODES = ["fp32", "tf32", "bf16", "fp16"]
 
 
 def _full_case(libgemm, oracle_cache, M, K, N, dist, mode):
@@ -61,7 +62,7 @@ def test_sweep_small_full(libgemm, oracle_cache, mode, n):
     _full_case(libgemm, oracle_cache, n, n, n, "u01", mode)
 
 
-@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16"])
 def test_same_inputs_diagnostic(libgemm, mode):
     """Tensor path against the oracle fed the very values the tensor cores
     read (TF32-exact or BF16 values): only binary32 accumulation differs."""
@@ -90,7 +91,7 @@ def test_sweep_large_sampled(libgemm, mode, n):
     _sampled_case(libgemm, n, n, n, "u01", mode)
 
 
-@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16"])
 def test_large_8192_sampled(libgemm, mode):
     _sampled_case(libgemm, 8192, 8192, 8192, "pm1", mode)
 
