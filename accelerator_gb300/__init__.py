@@ -6,9 +6,9 @@ loads nothing: the library is opened at the first call, and a missing library
 is an error, never a fallback.
 """
 
-FP32, TF32, BF16, FP16 = 0, 1, 2, 3
+FP32, TF32, BF16, FP16, FP32_VIA_BF16 = 0, 1, 2, 3, 4
 
-__all__ = ["gemm", "GemmError", "FP32", "TF32", "BF16", "FP16"]
+__all__ = ["gemm", "GemmError", "FP32", "TF32", "BF16", "FP16", "FP32_VIA_BF16"]
 
 
 def __getattr__(name):

@@ -12,8 +12,8 @@ import threading
 
 from . import build as _build
 
-FP32, TF32, BF16, FP16 = 0, 1, 2, 3
-MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16, "fp16": FP16}
+FP32, TF32, BF16, FP16, FP32_VIA_BF16 = 0, 1, 2, 3, 4
+MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16, "fp16": FP16, "fp32_via_bf16": FP32_VIA_BF16}
 
 OK = 0
 ERR_INVALID_ARG = 1

@@ -149,11 +149,46 @@ CUtensorMapDataType tensor_type(TcMode mode) {
                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
-                     int64_t N, DeviceState* st, cudaStream_t stream) {
+// The product on operands TMA can read: A (M x K, row stride lda) and B
+// (K x N, stride ldb) or, with b_k_major, B^T (N x K, stride ldb), with
+// 16-byte aligned bases and strides.
+int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const void* b_use,
+              int64_t ldb, float* C, int64_t M, int64_t K, int64_t N, DeviceState* st,
+              cudaStream_t stream) {
     const int es = mode == TcMode::kTF32 ? 4 : 2;
     const CUtensorMapDataType dt = tensor_type(mode);
     const TcShape shape = tc_shape(mode);
+    // The 2-SM kernel (CTA pairs) when the device can hold pair clusters; each
+    // CTA of a pair loads half of the B tile, so a K-major B box is half as tall.
+    const bool pairs = tc_max_pairs() > 0;
+    const int b_rows = pairs ? shape.block_n / 2 : shape.block_n;
+    CUtensorMap map_a, map_b;
+    int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m, dt);
+    if (rc == GEMM_OK)
+        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows, dt)
+                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt);
+    const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
+    CUtensorMap map_c;
+    const bool c_tma = pairs && c_vec && rc == GEMM_OK &&
+                       encode_2d(&map_c, C, 4, M, N, N, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) == GEMM_OK;
+    if (rc == GEMM_OK) {
+        const cudaError_t e =
+            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
+                                        (int)M, (int)N, (int)K, c_vec, st->err, kWaitLimitNs, stream)
+                  : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
+                                   st->num_sms, st->err, kWaitLimitNs, stream);
+        if (e != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        else
+            g_launches++;
+    }
+    return rc;
+}
+
+int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
+                     int64_t N, DeviceState* st, cudaStream_t stream) {
+    const int es = mode == TcMode::kTF32 ? 4 : 2;
     const int64_t align_elems = 16 / es;
     // BF16 reads B as an MN-major operand, straight from the caller's K x N
     // rows.  The MN-major form of kind::tf32 returned zeros on GB300, so the
@@ -197,32 +232,33 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
         }
     }
 
-    // The 2-SM kernel (CTA pairs) when the device can hold pair clusters; each
-    // CTA of a pair loads half of the B tile, so a K-major B box is half as tall.
-    const bool pairs = tc_max_pairs() > 0;
-    const int b_rows = pairs ? shape.block_n / 2 : shape.block_n;
-    CUtensorMap map_a, map_b;
-    int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m, dt);
-    if (rc == GEMM_OK)
-        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows, dt)
-                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt);
-    const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
-    // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
-    CUtensorMap map_c;
-    const bool c_tma = pairs && c_vec && rc == GEMM_OK &&
-                       encode_2d(&map_c, C, 4, M, N, N, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) == GEMM_OK;
-    if (rc == GEMM_OK) {
-        const cudaError_t e =
-            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
-                                        (int)M, (int)N, (int)K, c_vec, st->err, kWaitLimitNs, stream)
-                  : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
-                                   st->num_sms, st->err, kWaitLimitNs, stream);
-        if (e != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        else
-            g_launches++;
-    }
+    int rc = tc_launch(mode, b_k_major, a_use, lda, b_use, ldb, C, M, K, N, st, stream);
     if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
+    return rc;
+}
+
+// GEMM_FP32_VIA_BF16: round A and B to bfloat16 into scratch rows whose
+// stride is a multiple of 16 bytes (TMA-ready), then the BF16 product.
+int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
+                      DeviceState* st, cudaStream_t stream) {
+    const int64_t lda = round_up(K, 8), ldb = round_up(N, 8);
+    const int64_t a_bytes = round_up(M * lda * 2, 256), b_bytes = round_up(K * ldb * 2, 256);
+    void* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes), st->pool, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_MEMORY;
+    }
+    uint8_t* s = static_cast<uint8_t*>(scratch);
+    int rc = GEMM_OK;
+    if (launch_to_bf16(A, s, M, K, lda, stream) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    g_launches++;
+    if (rc == GEMM_OK && launch_to_bf16(B, s + a_bytes, K, N, ldb, stream) != cudaSuccess)
+        rc = GEMM_ERR_CUDA;
+    g_launches++;
+    if (rc == GEMM_OK)
+        rc = tc_launch(TcMode::kBF16, false, s, lda, s + a_bytes, ldb, C, M, K, N, st, stream);
+    if (cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }
 
@@ -257,7 +293,7 @@ int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N
          int precision_mode, struct CUstream_st* stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16 &&
-        precision_mode != GEMM_FP16)
+        precision_mode != GEMM_FP16 && precision_mode != GEMM_FP32_VIA_BF16)
         return GEMM_ERR_INVALID_ARG;
     if (M < 0 || K < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
     // Every dimension must fit the kernels' 32-bit indices and TMA coordinates.
@@ -289,6 +325,9 @@ int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N
     if (precision_mode == GEMM_FP32) return ffma_gemm(static_cast<const float*>(A),
                                                       static_cast<const float*>(B), C, M, K, N, st,
                                                       stream);
+    if (precision_mode == GEMM_FP32_VIA_BF16)
+        return rounded_bf16_gemm(static_cast<const float*>(A), static_cast<const float*>(B), C, M,
+                                 K, N, st, stream);
     const TcMode tm = precision_mode == GEMM_BF16   ? TcMode::kBF16
                       : precision_mode == GEMM_FP16 ? TcMode::kF16
                                                     : TcMode::kTF32;

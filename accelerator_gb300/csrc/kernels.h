@@ -58,6 +58,10 @@ cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t co
 // dst (cols x rows, row stride dst_ld elements) = transpose of src (rows x cols, dense).
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
                              int64_t dst_ld, int es, cudaStream_t stream);
+// dst (rows x cols bfloat16, row stride dst_ld elements) = round-to-nearest-
+// even of src (rows x cols float, dense).
+cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,
+                           int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 

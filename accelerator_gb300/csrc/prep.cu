@@ -6,6 +6,8 @@
 //   fill_zero   C := 0 for K == 0 (the empty sum).
 //   wait_selftest  one CTA waits on an mbarrier that nothing completes, to
 //               show the bounded wait gives up and reports instead of hanging.
+#include <cuda_bf16.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -87,6 +89,30 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
     }
 }
 
+// float -> bfloat16, round to nearest even, into rows of stride dst_ld.  The
+// vector form reads 4 floats (16 bytes) and writes 4 bf16 (8 bytes) per step;
+// it needs cols % 4 == 0, 16-byte aligned src and 8-byte aligned dst rows.
+__global__ void to_bf16_v4_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                  int64_t rows, int64_t cols4, int64_t dst_ld4) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols4;
+             c += (int64_t)gridDim.x * blockDim.x) {
+            const float4 v = src[r * cols4 + c];
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+            dst[r * dst_ld4 + c] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                              *reinterpret_cast<const uint32_t*>(&hi));
+        }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                               int64_t rows, int64_t cols, int64_t dst_ld) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x)
+            dst[r * dst_ld + c] = __float2bfloat16_rn(src[r * cols + c]);
+}
+
 __global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
@@ -151,6 +177,26 @@ cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t c
             static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, dst_ld);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,
+                           int64_t dst_ld, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int threads = 256;
+    const unsigned gy = (unsigned)(rows < 65535 ? rows : 65535);
+    if (cols % 4 == 0 && dst_ld % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+        const int64_t c4 = cols / 4, bx = (c4 + threads - 1) / threads;
+        dim3 grid((unsigned)(bx < 16 ? bx : 16), gy);
+        to_bf16_v4_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                        static_cast<uint2*>(dst), rows, c4, dst_ld / 4);
+    } else {
+        const int64_t bx = (cols + threads - 1) / threads;
+        dim3 grid((unsigned)(bx < 64 ? bx : 64), gy);
+        to_bf16_kernel<<<grid, threads, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), rows,
+                                                     cols, dst_ld);
+    }
     return cudaGetLastError();
 }
 

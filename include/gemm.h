@@ -56,7 +56,12 @@ enum gemm_mode {
      * (tcgen05, kind::f16 with F16 inputs), binary32 accumulation -- the
      * FP16-input, FP32-accumulate product the first page's "Further
      * Optimisation Ideas" names for tensor cores. */
-    GEMM_FP16 = 3
+    GEMM_FP16 = 3,
+    /* A, B: const float*.  The library rounds them to bfloat16 (to nearest,
+     * ties to even) in a conversion pass, then multiplies as GEMM_BF16:
+     * BF16 tensor-core speed for float data, at BF16 input precision.  The
+     * result equals GEMM_BF16 on the caller-rounded operands, bit for bit. */
+    GEMM_FP32_VIA_BF16 = 4
 };
 
 /* Status codes returned by every entry point (0 = success). */
@@ -86,6 +91,8 @@ enum gemm_status {
  *                   K == 0: C is set to 0 (the empty sum).
  *   precision_mode  one of enum gemm_mode
  *   stream          stream to enqueue on
+ * GEMM_FP32_VIA_BF16 takes scratch for the rounded copies of A and B, from the
+ * same stream-ordered allocator.
  * Any alignment of element size or more is accepted.  When a tensor-core mode
  * meets a row stride that is not a multiple of 16 bytes, or a base address
  * that is not 16-byte aligned, the operand is first copied into a scratch

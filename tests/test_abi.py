@@ -38,7 +38,7 @@ def test_status_strings(libgemm):
     assert libgemm.launch_count() >= 0
 
 
-@pytest.mark.parametrize("mode", [-1, 4, 17])
+@pytest.mark.parametrize("mode", [-1, 5, 17])
 def test_bad_mode(libgemm, mode):
     assert libgemm.gemm_raw(FAKE, FAKE + 4096, FAKE + 8192, 4, 4, 4, mode) == libgemm.ERR_INVALID_ARG
 

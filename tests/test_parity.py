@@ -114,3 +114,17 @@ def test_fp32_fma_chain_hand_cases(libgemm):
         B = case["B"].astype(np.float32).reshape(-1, 1)
         C = run(libgemm, A, B, "fp32")
         assert float(C[0, 0]) == float(case["C"][0]), case["name"]
+
+
+@pytest.mark.parametrize("M,K,N", [(1000, 777, 1500), (4096, 4096, 4096), (129, 65, 257), (1, 1, 1)])
+def test_fp32_via_bf16_equals_bf16_on_rounded_operands(libgemm, M, K, N):
+    """GEMM_FP32_VIA_BF16 rounds float operands to bfloat16 on the GPU (to
+    nearest, ties to even) and multiplies as GEMM_BF16: bit for bit the same
+    as GEMM_BF16 on operands rounded on the host, and within the BF16
+    tolerance of the oracle on the original floats."""
+    A, B = inputs.matrices(M, K, N, "pm1", seed=M + K + N)
+    C = run(libgemm, A, B, "fp32_via_bf16")
+    np.testing.assert_array_equal(C, run(libgemm, A, B, "bf16"))
+    if M * N * K <= 2 ** 31:
+        Cref, S = oracle.gemm(A, B)
+        assert_within(C, Cref, S, TOL["fp32_via_bf16"], "fp32 via bf16")
