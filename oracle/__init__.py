@@ -65,6 +65,10 @@ def _load():
             lib.oracle_threads.argtypes = [ip]
             lib.oracle_gemm_f32_chain.argtypes = [vp, vp, i64, i64, i64, vp, ip]
             lib.oracle_gemm_f32_chain.restype = ctypes.c_int
+            lib.oracle_update.argtypes = [vp, vp, i64, ctypes.c_double, ctypes.c_double, vp]
+            lib.oracle_update.restype = ctypes.c_int
+            lib.oracle_update_f32.argtypes = [vp, vp, i64, ctypes.c_float, ctypes.c_float, vp]
+            lib.oracle_update_f32.restype = ctypes.c_int
             for f in (lib.oracle_gemm, lib.oracle_dot, lib.oracle_sum,
                       lib.oracle_widen, lib.oracle_threads):
                 f.restype = ctypes.c_int
@@ -160,4 +164,38 @@ def widen(x: np.ndarray, fmt: str) -> np.ndarray:
     rc = _load().oracle_widen(_FMT[fmt], _ptr(x), x.size, _ptr(out))
     if rc != 0:
         raise RuntimeError("oracle_widen failed")
+    return out
+
+
+def update(P, C_in, alpha: float, beta: float) -> np.ndarray:
+    """alpha * P + beta * C_in in double (P the product, C_in the old C).
+
+    beta == 0 reads no C_in and alpha == 0 reads no P: pass None there.
+    """
+    ref = P if P is not None else C_in
+    shape = np.shape(ref)
+    n = int(np.prod(shape))
+    Pd = None if P is None else np.ascontiguousarray(P, dtype=np.float64)
+    Cf = None if C_in is None else np.ascontiguousarray(C_in, dtype=np.float32)
+    out = np.empty(shape, np.float64)
+    rc = _load().oracle_update(None if Pd is None else _ptr(Pd), None if Cf is None else _ptr(Cf),
+                               n, float(alpha), float(beta), _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_update failed")
+    return out
+
+
+def update_f32(P, C_in, alpha: float, beta: float) -> np.ndarray:
+    """The binary32 update fmaf(beta, C_in, alpha * P) (see oracle_update_f32)."""
+    ref = P if P is not None else C_in
+    shape = np.shape(ref)
+    n = int(np.prod(shape))
+    Pf = None if P is None else np.ascontiguousarray(P, dtype=np.float32)
+    Cf = None if C_in is None else np.ascontiguousarray(C_in, dtype=np.float32)
+    out = np.empty(shape, np.float32)
+    rc = _load().oracle_update_f32(None if Pf is None else _ptr(Pf),
+                                   None if Cf is None else _ptr(Cf), n, float(alpha), float(beta),
+                                   _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_update_f32 failed")
     return out

@@ -15,6 +15,9 @@
  *     is C[i*N + j]; there are no leading-dimension arguments.
  *   - The sum-of-all-elements check in double precision: "From 306 ms to
  *     86 ms" (kpapadogiannis.dev), the "How each kernel was timed" box.
+ *   - The generalised product C := alpha*A*B + beta*C: "Matrix
+ *     Multiplication -- Naive to Tiled", section 07, the cuBLAS comparison
+ *     call (oracle_update, oracle_update_f32).
  *
  * Readings taken where the pages are silent (each is also listed in the
  * design notes):
@@ -43,6 +46,11 @@
  * and rounding of the sum open; this is the reading the library's FP32 mode
  * documents, and tests compare it bit for bit where the library does not split
  * the K range.
+ *
+ * The update's pins: hand-worked cases (tests/golden/update_hand.txt),
+ * alpha = 1 / beta = 0 giving the product, beta = 0 ignoring a NaN C, alpha
+ * = 0 ignoring a NaN product, a tie that shows alpha*P is rounded once, and a
+ * case whose fused and unfused results differ.
  *
  * Parity pins (tests/test_oracle.py): identity and permutation matrices,
  * hand-worked integer products (tests/golden/), rank-1 closed forms, all-ones
@@ -245,6 +253,50 @@ int oracle_gemm_f32_chain(const float* A, const float* B, int64_t M, int64_t K, 
             float acc = 0.0f;
             for (int64_t k = 0; k < K; ++k) acc = fmaf(A[i * K + k], B[k * N + j], acc);
             C[i * N + j] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The update C := alpha * P + beta * C_in of the generalised product, with P
+ * the product A*B ("Matrix Multiplication -- Naive to Tiled", section 07, the
+ * cuBLAS comparison call, whose comment states C = alpha*A*B + beta*C), in
+ * double, element by element over n entries.  BLAS conventions where the
+ * page is silent: beta == 0 reads no C_in (it may be NULL, and a NaN there
+ * does not propagate); alpha == 0 reads no P (the product is not needed).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_update(const double* P, const float* C_in, int64_t n, double alpha, double beta,
+                  double* out) {
+    if (n < 0 || (n > 0 && (!out || (alpha != 0.0 && !P) || (beta != 0.0 && !C_in))))
+        return -1;
+    for (int64_t t = 0; t < n; ++t) {
+        double v = alpha != 0.0 ? alpha * P[t] : 0.0;
+        if (beta != 0.0) v += beta * (double)C_in[t];
+        out[t] = v;
+    }
+    return 0;
+}
+
+/*
+ * The same update as a binary32 machine computes it from the binary32 sum P:
+ * t = alpha * P rounded once, then out = fmaf(beta, C_in, t) (one fused
+ * multiply-add, rounded once).  beta == 0 gives t without reading C_in;
+ * alpha == 0 gives beta * C_in rounded once (0 when beta == 0 as well),
+ * without reading P.  This is the reading the library's binary32 epilogue
+ * documents; the page leaves the rounding open.
+ */
+int oracle_update_f32(const float* P, const float* C_in, int64_t n, float alpha, float beta,
+                      float* out) {
+    if (n < 0 || (n > 0 && (!out || (alpha != 0.0f && !P) || (beta != 0.0f && !C_in))))
+        return -1;
+    for (int64_t t = 0; t < n; ++t) {
+        if (alpha == 0.0f) {
+            out[t] = beta != 0.0f ? beta * C_in[t] : 0.0f;
+        } else {
+            const float s = alpha * P[t];
+            out[t] = beta != 0.0f ? fmaf(beta, C_in[t], s) : s;
         }
     }
     return 0;

@@ -47,3 +47,33 @@ def page_gflops():
             dec = len(ms.split(".")[1]) if "." in ms else 0
             rows.append((int(n), float(ms), float(gf.replace(",", "")), dec))
     return rows
+
+
+def update_hand():
+    """Parse update_hand.txt into dicts {name, dims, alpha, beta, A, B, C_in, OUT}."""
+    cases = []
+    cur = None
+    block = None
+    with open(os.path.join(GOLDEN, "update_hand.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                _, name, m, k, n, alpha, beta = line.split()
+                cur = {"name": name, "dims": (int(m), int(k), int(n)),
+                       "alpha": float(alpha), "beta": float(beta)}
+                cases.append(cur)
+                block = None
+            elif line in ("A", "B", "C_in", "OUT"):
+                block = line
+                cur[block] = []
+            else:
+                cur[block].append([float(v) for v in line.split()])
+    for c in cases:
+        for key in ("A", "B", "C_in", "OUT"):
+            c[key] = np.asarray(c[key], np.float64)
+        m, k, n = c["dims"]
+        assert c["A"].shape == (m, k) and c["B"].shape == (k, n)
+        assert c["C_in"].shape == (m, n) and c["OUT"].shape == (m, n)
+    return cases

@@ -21,7 +21,7 @@ import pytest
 
 import oracle
 from accelerator_gb300 import inputs
-from golden_io import hand_products
+from golden_io import hand_products, update_hand
 
 
 def _f32(x):
@@ -267,3 +267,77 @@ def test_f32_chain_within_binary32_bound():
     g = 300 * u / (1 - 300 * u)
     assert np.all(np.abs(C - ref) <= g * S)
     assert np.any(C != ref)            # it really is binary32 arithmetic
+
+
+# ---- the update C := alpha * A*B + beta * C_in (generalised product) ----
+
+@pytest.mark.parametrize("case", update_hand(), ids=lambda c: c["name"])
+def test_update_hand_cases(case):
+    P, _ = oracle.gemm(case["A"], case["B"], "f64")
+    out = oracle.update(P, case["C_in"], case["alpha"], case["beta"])
+    np.testing.assert_array_equal(out, case["OUT"])
+    P32 = P.astype(np.float32)
+    out32 = oracle.update_f32(P32, case["C_in"], case["alpha"], case["beta"])
+    np.testing.assert_array_equal(out32.astype(np.float64), case["OUT"])   # exact in binary32
+
+
+def test_update_identity_and_empty():
+    P = np.arange(12, dtype=np.float64).reshape(3, 4) - 5.5
+    np.testing.assert_array_equal(oracle.update(P, None, 1.0, 0.0), P)
+    np.testing.assert_array_equal(oracle.update_f32(P, None, 1.0, 0.0), P.astype(np.float32))
+    assert oracle.update(np.zeros((0, 3)), None, 2.0, 0.0).shape == (0, 3)
+
+
+def test_update_beta_zero_reads_no_c():
+    P = np.array([[1.0, -2.0], [3.0, 0.5]])
+    nan_c = np.full((2, 2), np.nan, np.float32)
+    out = oracle.update(P, nan_c, 3.0, 0.0)
+    np.testing.assert_array_equal(out, 3.0 * P)
+    out32 = oracle.update_f32(P, nan_c, 3.0, 0.0)
+    np.testing.assert_array_equal(out32, (3.0 * P).astype(np.float32))
+
+
+def test_update_alpha_zero_reads_no_product():
+    C_in = np.array([[1.5, -2.0, np.inf]], np.float32)
+    P = np.full((1, 3), np.nan)
+    np.testing.assert_array_equal(oracle.update(P, C_in, 0.0, -2.0), [[-3.0, 4.0, -np.inf]])
+    np.testing.assert_array_equal(oracle.update_f32(P, C_in, 0.0, -2.0), [[-3.0, 4.0, -np.inf]])
+    np.testing.assert_array_equal(oracle.update(None, C_in, 0.0, 0.0), np.zeros((1, 3)))
+
+
+def test_update_f32_rounds_alpha_product_once():
+    # alpha * P = 3 * (1 + 2^-23) = 3 + 1.5 * 2^-22 lies halfway between the
+    # binary32 neighbours 3 + 2^-22 (odd) and 3 + 2^-21 (even): ties to even.
+    P = np.array([1.0 + 2.0 ** -23], np.float32)
+    out = oracle.update_f32(P, None, 3.0, 0.0)
+    assert float(out[0]) == 3.0 + 2.0 ** -21
+    C_in = P.copy()                       # alpha = 0: beta * C_in, the same rounding
+    assert float(oracle.update_f32(None, C_in, 0.0, 3.0)[0]) == 3.0 + 2.0 ** -21
+
+
+def test_update_f32_is_fused():
+    # beta * C_in = (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 exactly; with t = -1 the
+    # fused result is 2^-11 + 2^-24.  Rounding beta * C_in first (a tie, to
+    # the even 1 + 2^-11) would give 2^-11.
+    b = 1.0 + 2.0 ** -12
+    out = oracle.update_f32(np.array([-1.0], np.float32), np.array([b], np.float32), 1.0, b)
+    assert float(out[0]) == 2.0 ** -11 + 2.0 ** -24
+
+
+def test_update_f32_within_two_roundings_of_exact():
+    rng = np.random.default_rng(21)
+    P = rng.standard_normal(1000).astype(np.float32)
+    C_in = rng.standard_normal(1000).astype(np.float32)
+    alpha, beta = np.float32(0.7), np.float32(-1.3)
+    out = oracle.update_f32(P, C_in, alpha, beta).astype(np.float64)
+    exact = oracle.update(P.astype(np.float64), C_in, float(alpha), float(beta))
+    u = 2.0 ** -24
+    bound = 2 * u * (np.abs(float(alpha) * P.astype(np.float64)) + np.abs(exact)) + 1e-45
+    assert np.all(np.abs(out - exact) <= bound)
+
+
+def test_update_rejects_missing_operands():
+    with pytest.raises(RuntimeError):
+        oracle.update(None, np.ones((2, 2), np.float32), 1.0, 1.0)
+    with pytest.raises(RuntimeError):
+        oracle.update_f32(np.ones((2, 2), np.float32), None, 1.0, 1.0)
