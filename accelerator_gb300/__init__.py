@@ -8,11 +8,11 @@ is an error, never a fallback.
 
 FP32, TF32, BF16, FP16, FP32_VIA_BF16 = 0, 1, 2, 3, 4
 
-__all__ = ["gemm", "GemmError", "FP32", "TF32", "BF16", "FP16", "FP32_VIA_BF16"]
+__all__ = ["gemm", "gemm_ex", "GemmError", "FP32", "TF32", "BF16", "FP16", "FP32_VIA_BF16"]
 
 
 def __getattr__(name):
-    if name in ("gemm", "GemmError"):
+    if name in ("gemm", "gemm_ex", "GemmError"):
         from . import binding
         return getattr(binding, name)
     raise AttributeError(name)

@@ -28,6 +28,8 @@ ERR_SCRATCH_LIMIT = 7
 _i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "gemm": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "gemm_ex": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, ctypes.c_float, _int,
+                       _vp]),
     "gemm_status_string": (ctypes.c_char_p, [_int]),
     "gemm_debug_status": (_int, [_vp]),
     "gemm_version": (_int, []),
@@ -76,6 +78,13 @@ def gemm_raw(a_ptr: int, b_ptr: int, c_ptr: int, M: int, K: int, N: int, mode: i
                           stream_ptr or None))
 
 
+def gemm_ex_raw(a_ptr: int, b_ptr: int, c_ptr: int, M: int, K: int, N: int, alpha: float,
+                beta: float, mode: int, stream_ptr: int = 0) -> int:
+    """Direct call of gemm_ex with raw addresses; returns the status."""
+    return int(lib().gemm_ex(a_ptr or None, b_ptr or None, c_ptr or None, M, K, N, float(alpha),
+                             float(beta), mode, stream_ptr or None))
+
+
 def _stream_ptr(stream) -> int:
     import torch
     if stream is None:
@@ -91,6 +100,31 @@ def gemm(A, B, C=None, mode=FP32, stream=None):
     overwrite, or None to allocate one.  Returns C.  Asynchronous on `stream`
     (default: torch's current stream).
     """
+    mode, C = _operands(A, B, C, mode)
+    rc = gemm_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), A.shape[0], A.shape[1], B.shape[1],
+                  mode, _stream_ptr(stream))
+    if rc != OK:
+        raise GemmError(rc)
+    return C
+
+
+def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, mode=FP32, stream=None):
+    """C = alpha * A @ B + beta * C with libgemm (operands as for gemm()).
+
+    C is read when beta != 0; with C None, beta must be 0.  Returns C.
+    """
+    if C is None and beta != 0:
+        raise ValueError("beta != 0 needs an input C")
+    mode, C = _operands(A, B, C, mode)
+    rc = gemm_ex_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), A.shape[0], A.shape[1],
+                     B.shape[1], alpha, beta, mode, _stream_ptr(stream))
+    if rc != OK:
+        raise GemmError(rc, "gemm_ex")
+    return C
+
+
+def _operands(A, B, C, mode):
+    """Checks the tensors of a call; returns (mode number, C or a new C)."""
     import torch
     if isinstance(mode, str):
         mode = MODES[mode.lower()]
@@ -107,10 +141,7 @@ def gemm(A, B, C=None, mode=FP32, stream=None):
     elif (C.dtype != torch.float32 or not C.is_cuda or not C.is_contiguous()
           or tuple(C.shape) != (M, N)):
         raise TypeError("C must be a contiguous CUDA float32 tensor of shape (M, N)")
-    rc = gemm_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, K, N, mode, _stream_ptr(stream))
-    if rc != OK:
-        raise GemmError(rc)
-    return C
+    return mode, C
 
 
 def debug_status(stream=None) -> int:

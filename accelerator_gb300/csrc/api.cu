@@ -111,7 +111,7 @@ int encode_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t c
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
-              DeviceState* st, cudaStream_t stream) {
+              const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
     const bool b_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
     const FfmaPlan plan = ffma_plan((int)M, (int)N, (int)K, st->num_sms);
@@ -135,7 +135,7 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
     }
     int rc = GEMM_OK;
     if (launch_ffma_sgemm(A, B, C, (int)M, (int)N, (int)K, b_vec, c_vec, plan, partial, counters,
-                          stream) != cudaSuccess)
+                          epi, stream) != cudaSuccess)
         rc = GEMM_ERR_CUDA;
     else
         g_launches++;
@@ -153,8 +153,8 @@ CUtensorMapDataType tensor_type(TcMode mode) {
 // (K x N, stride ldb) or, with b_k_major, B^T (N x K, stride ldb), with
 // 16-byte aligned bases and strides.
 int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const void* b_use,
-              int64_t ldb, float* C, int64_t M, int64_t K, int64_t N, DeviceState* st,
-              cudaStream_t stream) {
+              int64_t ldb, float* C, int64_t M, int64_t K, int64_t N, const Epilogue& epi,
+              DeviceState* st, cudaStream_t stream) {
     const int es = mode == TcMode::kTF32 ? 4 : 2;
     const CUtensorMapDataType dt = tensor_type(mode);
     const TcShape shape = tc_shape(mode);
@@ -175,9 +175,10 @@ int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const
     if (rc == GEMM_OK) {
         const cudaError_t e =
             pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
-                                        (int)M, (int)N, (int)K, c_vec, st->err, kWaitLimitNs, stream)
+                                        (int)M, (int)N, (int)K, c_vec, epi, st->err, kWaitLimitNs,
+                                        stream)
                   : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
-                                   st->num_sms, st->err, kWaitLimitNs, stream);
+                                   epi, st->num_sms, st->err, kWaitLimitNs, stream);
         if (e != cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
@@ -187,7 +188,7 @@ int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const
 }
 
 int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
-                     int64_t N, DeviceState* st, cudaStream_t stream) {
+                     int64_t N, const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
     const int es = mode == TcMode::kTF32 ? 4 : 2;
     const int64_t align_elems = 16 / es;
     // BF16 reads B as an MN-major operand, straight from the caller's K x N
@@ -232,7 +233,7 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
         }
     }
 
-    int rc = tc_launch(mode, b_k_major, a_use, lda, b_use, ldb, C, M, K, N, st, stream);
+    int rc = tc_launch(mode, b_k_major, a_use, lda, b_use, ldb, C, M, K, N, epi, st, stream);
     if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }
@@ -240,7 +241,7 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
 // GEMM_FP32_VIA_BF16: round A and B to bfloat16 into scratch rows whose
 // stride is a multiple of 16 bytes (TMA-ready), then the BF16 product.
 int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
-                      DeviceState* st, cudaStream_t stream) {
+                      const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
     const int64_t lda = round_up(K, 8), ldb = round_up(N, 8);
     const int64_t a_bytes = round_up(M * lda * 2, 256), b_bytes = round_up(K * ldb * 2, 256);
     void* scratch = nullptr;
@@ -257,7 +258,7 @@ int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64
         rc = GEMM_ERR_CUDA;
     g_launches++;
     if (rc == GEMM_OK)
-        rc = tc_launch(TcMode::kBF16, false, s, lda, s + a_bytes, ldb, C, M, K, N, st, stream);
+        rc = tc_launch(TcMode::kBF16, false, s, lda, s + a_bytes, ldb, C, M, K, N, epi, st, stream);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }
@@ -287,11 +288,11 @@ void count_launch() { g_launches++; }
 
 }  // namespace libgemm
 
-extern "C" {
+namespace {
 
-int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
-         int precision_mode, struct CUstream_st* stream_) {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+// Validation and dispatch shared by gemm() and gemm_ex().
+int gemm_impl(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
+              float alpha, float beta, int precision_mode, cudaStream_t stream) {
     if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16 &&
         precision_mode != GEMM_FP16 && precision_mode != GEMM_FP32_VIA_BF16)
         return GEMM_ERR_INVALID_ARG;
@@ -317,21 +318,43 @@ int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N
     int rc = device_state(&st);
     if (rc != GEMM_OK) return rc;
 
-    if (K == 0) {
-        if (launch_fill_zero(C, M * N, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    // K == 0 (the empty sum) or alpha == 0: C := beta * C, and A, B are not
+    // read; beta == 0 gives 0 without reading C, beta == 1 leaves C as it is.
+    if (K == 0 || alpha == 0.0f) {
+        if (beta == 1.0f) return GEMM_OK;
+        const cudaError_t e = beta == 0.0f ? launch_fill_zero(C, M * N, stream)
+                                           : launch_scale(C, M * N, beta, stream);
+        if (e != cudaSuccess) return GEMM_ERR_CUDA;
         g_launches++;
         return GEMM_OK;
     }
+    const Epilogue epi{alpha, beta, beta != 0.0f ? 2 : (alpha != 1.0f ? 1 : 0)};
     if (precision_mode == GEMM_FP32) return ffma_gemm(static_cast<const float*>(A),
-                                                      static_cast<const float*>(B), C, M, K, N, st,
-                                                      stream);
+                                                      static_cast<const float*>(B), C, M, K, N, epi,
+                                                      st, stream);
     if (precision_mode == GEMM_FP32_VIA_BF16)
         return rounded_bf16_gemm(static_cast<const float*>(A), static_cast<const float*>(B), C, M,
-                                 K, N, st, stream);
+                                 K, N, epi, st, stream);
     const TcMode tm = precision_mode == GEMM_BF16   ? TcMode::kBF16
                       : precision_mode == GEMM_FP16 ? TcMode::kF16
                                                     : TcMode::kTF32;
-    return tensor_core_gemm(tm, A, B, C, M, K, N, st, stream);
+    return tensor_core_gemm(tm, A, B, C, M, K, N, epi, st, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
+         int precision_mode, struct CUstream_st* stream) {
+    return gemm_impl(A, B, C, M, K, N, 1.0f, 0.0f, precision_mode,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N, float alpha,
+            float beta, int precision_mode, struct CUstream_st* stream) {
+    return gemm_impl(A, B, C, M, K, N, alpha, beta, precision_mode,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gemm_status_string(int status) {

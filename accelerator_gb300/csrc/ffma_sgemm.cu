@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     ffma_sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                       float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
                       int dp_tiles, int splits, float* __restrict__ partial,
-                      unsigned* __restrict__ counters) {
+                      unsigned* __restrict__ counters, const Epilogue epi) {
     constexpr int TM = CF::TM, TN = CF::TN, kStages = CF::kStages;
     extern __shared__ __align__(16) float smem[];
     float* sA = smem;                          // kStages x [kBK][kLdA]
@@ -333,13 +333,15 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
         for (int h = 0; h < TN / 4; ++h) {
             const int col = n0 + col_of(4 * h);
             if (kCVec && col < N) {   // N % 4 == 0: all four columns are in range
-                *reinterpret_cast<float4*>(crow + col) =
+                *reinterpret_cast<float4*>(crow + col) = epilogue_apply4(
+                    epi,
                     make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2),
-                                acc(i, 4 * h + 3));
+                                acc(i, 4 * h + 3)),
+                    crow + col);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (col + j < N) crow[col + j] = acc(i, 4 * h + j);
+                    if (col + j < N) crow[col + j] = epilogue_apply(epi, acc(i, 4 * h + j), crow + col + j);
             }
         }
     }
@@ -400,7 +402,7 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
 
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
                               bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, cudaStream_t stream) {
+                              unsigned* counters, const Epilogue& epi, cudaStream_t stream) {
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     if (plan.tiles <= 0) return cudaSuccess;
     const int64_t ctas = plan.dp_tiles + plan.split_tiles * plan.splits;
@@ -410,7 +412,7 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
     const size_t smem = FfmaCfg::kSmemBytes;
 #define LIBGEMM_FFMA_LAUNCH(BV, CV)                                                            \
     ffma_sgemm_kernel<FfmaCfg, BV, CV><<<grid, block, smem, stream>>>(                         \
-        A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters)
+        A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters, epi)
     if (b_vec && c_vec) LIBGEMM_FFMA_LAUNCH(true, true);
     else if (b_vec) LIBGEMM_FFMA_LAUNCH(true, false);
     else if (c_vec) LIBGEMM_FFMA_LAUNCH(false, true);

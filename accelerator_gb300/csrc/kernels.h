@@ -8,6 +8,38 @@
 
 namespace libgemm {
 
+// What every kernel does with a finished sum acc of C_ij:
+//   kind 0  C_ij := acc                          (C is not read)
+//   kind 1  C_ij := alpha * acc, rounded once    (C is not read)
+//   kind 2  C_ij := fma(beta, C_ij, alpha * acc), alpha * acc rounded first
+// -- the generalised product C = alpha*A*B + beta*C of the cuBLAS call in
+// "Matrix Multiplication -- Naive to Tiled", section 07.
+struct Epilogue {
+    float alpha, beta;
+    int kind;
+};
+constexpr Epilogue kPlainStore{1.0f, 0.0f, 0};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float epilogue_apply(const Epilogue& e, float acc, const float* c) {
+    if (e.kind == 0) return acc;
+    const float t = __fmul_rn(e.alpha, acc);
+    return e.kind == 1 ? t : __fmaf_rn(e.beta, *c, t);
+}
+// Four consecutive elements; c must be 16-byte aligned when e.kind == 2.
+__device__ __forceinline__ float4 epilogue_apply4(const Epilogue& e, float4 acc, const float* c) {
+    if (e.kind == 0) return acc;
+    float4 t = make_float4(__fmul_rn(e.alpha, acc.x), __fmul_rn(e.alpha, acc.y),
+                           __fmul_rn(e.alpha, acc.z), __fmul_rn(e.alpha, acc.w));
+    if (e.kind == 2) {
+        const float4 o = *reinterpret_cast<const float4*>(c);
+        t = make_float4(__fmaf_rn(e.beta, o.x, t.x), __fmaf_rn(e.beta, o.y, t.y),
+                        __fmaf_rn(e.beta, o.z, t.z), __fmaf_rn(e.beta, o.w, t.w));
+    }
+    return t;
+}
+#endif
+
 // ---- exact-FP32 CUDA-core GEMM (ffma_sgemm.cu) ----
 // b_vec: B rows may be copied 16 bytes at a time (N % 4 == 0, B 16-byte aligned).
 // c_vec: C rows may be stored 16 bytes at a time (N % 4 == 0, C 16-byte aligned).
@@ -23,7 +55,7 @@ cudaError_t ffma_setup();
 FfmaPlan ffma_plan(int M, int N, int K, int num_sms);
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
                               bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, cudaStream_t stream);
+                              unsigned* counters, const Epilogue& epi, cudaStream_t stream);
 
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
 enum class TcMode { kBF16, kTF32, kF16 };
@@ -43,12 +75,13 @@ int tc_max_pairs();
 // for TMA stores of the epilogue; without it C is stored by the threads.
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, unsigned* err, uint64_t limit_ns,
-                                cudaStream_t stream);
+                                int N, int K, bool c_vec, const Epilogue& epi, unsigned* err,
+                                uint64_t limit_ns, cudaStream_t stream);
 // b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
-                           int num_sms, unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+                           const Epilogue& epi, int num_sms, unsigned* err, uint64_t limit_ns,
+                           cudaStream_t stream);
 
 // ---- helpers (prep.cu) ----
 // Copy a rows x cols matrix of es-byte elements from row stride src_ld to
@@ -63,6 +96,8 @@ cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t c
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,
                            int64_t dst_ld, cudaStream_t stream);
 cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
+// C := beta * C over n elements, each rounded once (beta != 0).
+cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 // ---- host-side hooks of the C ABI (api.cu) ----

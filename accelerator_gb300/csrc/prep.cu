@@ -4,6 +4,7 @@
 //               of 16 bytes, for the tensor-core path when TMA cannot describe
 //               the caller's layout (e.g. K = 777 floats: 3108-byte rows).
 //   fill_zero   C := 0 for K == 0 (the empty sum).
+//   scale       C := beta * C, the generalised product when alpha == 0 or K == 0.
 //   wait_selftest  one CTA waits on an mbarrier that nothing completes, to
 //               show the bounded wait gives up and reports instead of hanging.
 #include <cuda_bf16.h>
@@ -119,6 +120,13 @@ __global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
         C[i] = 0.0f;
 }
 
+// C := beta * C, one rounding per element (alpha == 0 or K == 0 with beta != 0).
+__global__ void scale_kernel(float* __restrict__ C, int64_t n, float beta) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        C[i] = __fmul_rn(beta, C[i]);
+}
+
 __global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -204,6 +212,13 @@ cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
     int64_t blocks = (n + 255) / 256;
     fill_zero_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(C, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    scale_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(C, n, beta);
     return cudaGetLastError();
 }
 

@@ -94,11 +94,44 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
+// Applies the epilogue in place to one thread's 32 accumulator values: row
+// `row` of C, columns col0 .. col0 + 31.  Only kind 2 reads C, and only inside
+// M x N (16 bytes at a time when vec: C rows 16-byte aligned); values outside
+// are never stored.
+__device__ __forceinline__ void epilogue_row32(const Epilogue& e, uint32_t (&v)[32],
+                                               const float* crow, int row, int col0, int M,
+                                               int N, bool vec) {
+    if (e.kind == 0) return;
+    if (e.kind == 2 && row < M) {
+        if (vec && col0 + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 r = epilogue_apply4(
+                    e,
+                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])),
+                    crow + col0 + j);
+                v[j] = __float_as_uint(r.x), v[j + 1] = __float_as_uint(r.y);
+                v[j + 2] = __float_as_uint(r.z), v[j + 3] = __float_as_uint(r.w);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < N)
+                    v[j] = __float_as_uint(epilogue_apply(e, __uint_as_float(v[j]), crow + col0 + j));
+        }
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__fmul_rn(e.alpha, __uint_as_float(v[j])));
+}
+
 template <TcMode MODE, bool kBKMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, float* __restrict__ C, int M, int N,
-                   int K, int tiles_m, int tiles_n, int c_vec, unsigned* err, uint64_t limit_ns) {
+                   int K, int tiles_m, int tiles_n, int c_vec, const Epilogue epi, unsigned* err,
+                   uint64_t limit_ns) {
     using T = Traits<MODE>;
     constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
     constexpr int kUmmaK = 32 / T::kEs;                   // K per MMA: 16 / 8
@@ -254,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
+                epilogue_row32(epi, v, crow, row, col0, M, N, c_vec != 0);
                 if (row < M) {
                     if (c_vec && col0 + 32 <= N) {
 #pragma unroll
@@ -321,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c, float* __restrict__ C, int M,
-                        int N, int K, int pairs_m, int tiles_n, int c_mode, unsigned* err,
-                        uint64_t limit_ns) {
+                        int N, int K, int pairs_m, int tiles_n, int c_mode, const Epilogue epi,
+                        unsigned* err, uint64_t limit_ns) {
     using T = Traits<MODE>;
     constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
     constexpr int kUmmaK = 32 / T::kEs;                   // K per MMA: 16 / 8
@@ -495,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
+                epilogue_row32(epi, v, crow, row, col0, M, N, c_mode != kStoreScalar);
                 if (c_mode == kStoreTma) {
                     // Stage the warp's 32 x 32 block (row = lane) with the 128-byte
                     // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then
@@ -614,8 +649,8 @@ int tc_max_pairs() { return g_max_pairs; }
 
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, unsigned* err, uint64_t limit_ns,
-                                cudaStream_t stream) {
+                                int N, int K, bool c_vec, const Epilogue& epi, unsigned* err,
+                                uint64_t limit_ns, cudaStream_t stream) {
     const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
     const int64_t pairs = (int64_t)pairs_m * tiles_n;
     if (pairs <= 0) return cudaSuccess;
@@ -638,13 +673,13 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     cudaError_t e;
     if (mode == TcMode::kBF16 && !b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
     else if (mode == TcMode::kTF32 && b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
     else if (mode == TcMode::kF16 && !b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
     else
         return cudaErrorInvalidValue;
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -652,7 +687,8 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
 
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
-                           int num_sms, unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
+                           const Epilogue& epi, int num_sms, unsigned* err, uint64_t limit_ns,
+                           cudaStream_t stream) {
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     const int64_t tiles = (int64_t)tiles_m * tiles_n;
     if (tiles <= 0) return cudaSuccess;
@@ -661,7 +697,7 @@ cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a
     const int cv = c_vec ? 1 : 0;
 #define LIBGEMM_TC_LAUNCH(MODE_, BK_)                                                         \
     tc_gemm_kernel<MODE_, BK_><<<grid, kThreads, kSmemBytes, stream>>>(                      \
-        map_a, map_b, C, M, N, K, tiles_m, tiles_n, cv, err, limit_ns)
+        map_a, map_b, C, M, N, K, tiles_m, tiles_n, cv, epi, err, limit_ns)
     if (mode == TcMode::kBF16) {
         if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kBF16, true);
         else LIBGEMM_TC_LAUNCH(TcMode::kBF16, false);

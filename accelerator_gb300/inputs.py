@@ -46,6 +46,13 @@ def matrices(M: int, K: int, N: int, dist: str = "u01", seed: int = BASE_SEED):
     return _draw(ra, (M, K), dist), _draw(rb, (K, N), dist)
 
 
+def matrix_c(M: int, N: int, dist: str = "pm1", seed: int = BASE_SEED):
+    """An input C (M x N, row-major float32) for C = alpha*A*B + beta*C, from a
+    stream of its own (independent of the A and B of the same seed)."""
+    (rc,) = _streams(seed + 0x5EED, 1)
+    return _draw(rc, (M, N), dist)
+
+
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (to nearest, ties to even); uint16 patterns.
 

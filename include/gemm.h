@@ -103,6 +103,27 @@ enum gemm_status {
 GEMM_API int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
          int precision_mode, struct CUstream_st* stream);
 
+/*
+ * C = alpha*A*B + beta*C -- the generalised product of the cuBLAS call that
+ * "Matrix Multiplication -- Naive to Tiled" (section 07, Further Optimisation
+ * Ideas) uses as its yardstick, for the same row-major operands as gemm().
+ *   alpha, beta     binary32 scalars (host values)
+ *   other arguments as for gemm(); C is read as well as written when beta != 0
+ * Each C_ij is computed from the mode's sum acc_ij as fma(beta, C_ij, alpha *
+ * acc_ij), the product alpha * acc_ij rounded to binary32 first and the fused
+ * multiply-add rounded once.  Conventions of the BLAS, where the page is
+ * silent:
+ *   beta == 0       C is not read (NaN or garbage in C does not propagate);
+ *                   each C_ij := alpha * acc_ij.
+ *   alpha == 0, or K == 0   A and B are not read and no product is formed;
+ *                   C := beta * C (each element rounded once), C := 0 when
+ *                   beta == 0 as well, and nothing is enqueued when beta == 1.
+ *   alpha == 1, beta == 0   identical to gemm(), bit for bit.
+ * Validation, status codes, scratch use and asynchrony are those of gemm().
+ */
+GEMM_API int gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
+                     float alpha, float beta, int precision_mode, struct CUstream_st* stream);
+
 /* Static, human-readable name of a status code ("unknown status" otherwise). */
 GEMM_API const char* gemm_status_string(int status);
 

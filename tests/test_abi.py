@@ -90,3 +90,14 @@ def test_no_device_is_an_error_not_a_crash(libgemm):
     G = 1 << 20
     rc = libgemm.gemm_raw(FAKE, FAKE + G, FAKE + 2 * G, 4, 4, 4, 0)
     assert rc in (libgemm.ERR_CUDA, libgemm.ERR_UNSUPPORTED_DEVICE)
+
+
+def test_gemm_ex_validates_like_gemm(libgemm):
+    G = 1 << 20
+    ex = libgemm.gemm_ex_raw
+    assert ex(FAKE, FAKE + G, FAKE + 2 * G, 4, 4, 4, 2.0, 1.0, 5) == libgemm.ERR_INVALID_ARG
+    assert ex(FAKE, FAKE, FAKE, -1, 4, 4, 2.0, 1.0, 0) == libgemm.ERR_INVALID_ARG
+    assert ex(0, 0, 0, 0, 5, 5, 2.0, 1.0, 0) == libgemm.OK          # empty C: nothing to do
+    assert ex(0, FAKE + G, FAKE + 2 * G, 4, 4, 4, 2.0, 1.0, 0) == libgemm.ERR_INVALID_ARG
+    assert ex(FAKE, FAKE + G, FAKE + 2 * G + 2, 4, 4, 4, 2.0, 1.0, 1) == libgemm.ERR_MISALIGNED
+    assert ex(FAKE, FAKE + G, FAKE + 16, 4, 4, 4, 2.0, 1.0, 0) == libgemm.ERR_INVALID_ARG
