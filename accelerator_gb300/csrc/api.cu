@@ -251,12 +251,11 @@ int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64
         return GEMM_ERR_NO_MEMORY;
     }
     uint8_t* s = static_cast<uint8_t*>(scratch);
-    int rc = GEMM_OK;
-    if (launch_to_bf16(A, s, M, K, lda, stream) != cudaSuccess) rc = GEMM_ERR_CUDA;
-    g_launches++;
-    if (rc == GEMM_OK && launch_to_bf16(B, s + a_bytes, K, N, ldb, stream) != cudaSuccess)
+    int rc = GEMM_OK, launched = 0;
+    if (launch_to_bf16_pair(A, s, M, K, lda, B, s + a_bytes, K, N, ldb, stream, &launched) !=
+        cudaSuccess)
         rc = GEMM_ERR_CUDA;
-    g_launches++;
+    g_launches += launched;
     if (rc == GEMM_OK)
         rc = tc_launch(TcMode::kBF16, false, s, lda, s + a_bytes, ldb, C, M, K, N, epi, st, stream);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;

@@ -95,6 +95,12 @@ cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t c
 // even of src (rows x cols float, dense).
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,
                            int64_t dst_ld, cudaStream_t stream);
+// Both operands of GEMM_FP32_VIA_BF16 in one launch when their rows allow
+// 16-byte loads (cols % 4 == 0, 16-byte aligned src, ld % 4 == 0), else two
+// launch_to_bf16 calls; *launches receives the number of kernels enqueued.
+cudaError_t launch_to_bf16_pair(const float* a, void* a_dst, int64_t a_rows, int64_t a_cols,
+                                int64_t a_ld, const float* b, void* b_dst, int64_t b_rows,
+                                int64_t b_cols, int64_t b_ld, cudaStream_t stream, int* launches);
 cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
 // C := beta * C over n elements, each rounded once (beta != 0).
 cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream);

@@ -106,6 +106,46 @@ __global__ void to_bf16_v4_kernel(const float4* __restrict__ src, uint2* __restr
         }
 }
 
+// Both operands in one launch: rows [0, rows_a) of the combined index are
+// A's, the rest B's.  A block converts one row at a time, each thread four
+// 16-byte chunks per pass with all four loads issued before any store, so
+// about 64 bytes per thread are in flight (one chunk per thread leaves the
+// loads too few to cover HBM latency).  Needs the vector form's alignment.
+struct Bf16Job {
+    const float4* src;
+    uint2* dst;
+    int64_t rows, cols4, dst_ld4;
+};
+
+__global__ void __launch_bounds__(256) to_bf16_pair_kernel(Bf16Job a, Bf16Job b) {
+    const int64_t total = a.rows + b.rows;
+    for (int64_t rr = blockIdx.x; rr < total; rr += gridDim.x) {
+        const bool in_a = rr < a.rows;
+        const Bf16Job& j = in_a ? a : b;
+        const int64_t r = in_a ? rr : rr - a.rows;
+        const float4* s = j.src + r * j.cols4;
+        uint2* d = j.dst + r * j.dst_ld4;
+        for (int64_t c0 = threadIdx.x; c0 < j.cols4; c0 += 4 * (int64_t)blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t c = c0 + q * (int64_t)blockDim.x;
+                v[q] = c < j.cols4 ? __ldcs(s + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t c = c0 + q * (int64_t)blockDim.x;
+                if (c < j.cols4) {
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[q].x, v[q].y);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[q].z, v[q].w);
+                    d[c] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                      *reinterpret_cast<const uint32_t*>(&hi));
+                }
+            }
+        }
+    }
+}
+
 __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                int64_t rows, int64_t cols, int64_t dst_ld) {
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
@@ -205,6 +245,35 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t co
         to_bf16_kernel<<<grid, threads, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), rows,
                                                      cols, dst_ld);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16_pair(const float* a, void* a_dst, int64_t a_rows, int64_t a_cols,
+                                int64_t a_ld, const float* b, void* b_dst, int64_t b_rows,
+                                int64_t b_cols, int64_t b_ld, cudaStream_t stream, int* launches) {
+    auto vec_ok = [](const float* src, const void* dst, int64_t cols, int64_t ld) {
+        return cols % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+               (reinterpret_cast<uintptr_t>(dst) & 7u) == 0;
+    };
+    *launches = 0;
+    if (a_rows <= 0 || a_cols <= 0 || b_rows <= 0 || b_cols <= 0 ||
+        !vec_ok(a, a_dst, a_cols, a_ld) || !vec_ok(b, b_dst, b_cols, b_ld)) {
+        cudaError_t e = launch_to_bf16(a, a_dst, a_rows, a_cols, a_ld, stream);
+        ++*launches;
+        if (e == cudaSuccess) {
+            e = launch_to_bf16(b, b_dst, b_rows, b_cols, b_ld, stream);
+            ++*launches;
+        }
+        return e;
+    }
+    const Bf16Job ja{reinterpret_cast<const float4*>(a), static_cast<uint2*>(a_dst), a_rows,
+                     a_cols / 4, a_ld / 4};
+    const Bf16Job jb{reinterpret_cast<const float4*>(b), static_cast<uint2*>(b_dst), b_rows,
+                     b_cols / 4, b_ld / 4};
+    const int64_t rows = a_rows + b_rows;
+    const unsigned grid = (unsigned)(rows < (1 << 20) ? rows : (1 << 20));
+    to_bf16_pair_kernel<<<grid, 256, 0, stream>>>(ja, jb);
+    *launches = 1;
     return cudaGetLastError();
 }
 

@@ -54,3 +54,11 @@ def test_launch_count_counts_kernels(libgemm):
     libgemm.gemm(a2, b2, c, mode=libgemm.TF32)
     torch.cuda.synchronize()
     assert libgemm.launch_count() - n1 == 3
+    # FP32_VIA_BF16: one conversion kernel for both operands + MMA kernel when
+    # their rows are whole 16-byte chunks; two conversion kernels otherwise
+    n2 = libgemm.launch_count()
+    libgemm.gemm(a, b, c, mode=libgemm.FP32_VIA_BF16)
+    assert libgemm.launch_count() - n2 == 2
+    libgemm.gemm(a2, b2, c, mode=libgemm.FP32_VIA_BF16)
+    torch.cuda.synchronize()
+    assert libgemm.launch_count() - n2 == 5

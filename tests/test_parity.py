@@ -116,7 +116,8 @@ def test_fp32_fma_chain_hand_cases(libgemm):
         assert float(C[0, 0]) == float(case["C"][0]), case["name"]
 
 
-@pytest.mark.parametrize("M,K,N", [(1000, 777, 1500), (4096, 4096, 4096), (129, 65, 257), (1, 1, 1)])
+@pytest.mark.parametrize("M,K,N", [(1000, 777, 1500), (4096, 4096, 4096), (129, 65, 257), (1, 1, 1),
+                                   (640, 96, 1028), (3, 4, 4)])
 def test_fp32_via_bf16_equals_bf16_on_rounded_operands(libgemm, M, K, N):
     """GEMM_FP32_VIA_BF16 rounds float operands to bfloat16 on the GPU (to
     nearest, ties to even) and multiplies as GEMM_BF16: bit for bit the same
