@@ -73,10 +73,27 @@ int tc_max_pairs();
 // bytes (MN-major) or 128 rows x 128 bytes (K-major), i.e. block_n / 2 wide.
 // map_c (may be null): C as a 2-D fp32 tensor, box 32 x 32, 128-byte swizzle,
 // for TMA stores of the epilogue; without it C is stored by the threads.
+// K split of the pair kernel: splits units per pair tile, each over
+// k_per_split K slabs (k_elems each; the last unit takes the rest, and every
+// unit has at least one), storing raw partials through map_c into a
+// workspace of splits blocks of ws_rows rows (ws_rows a multiple of 256).
+struct TcSplit {
+    int splits, k_per_split, ws_rows;
+};
+constexpr TcSplit kNoSplit{1, 0, 0};
+// The split the pair kernel should use for an M x K x N product (kNoSplit
+// when the tiles alone fill the GPU, or splitting would not pay).
+TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, const Epilogue& epi, unsigned* err,
-                                uint64_t limit_ns, cudaStream_t stream);
+                                int N, int K, bool c_vec, const Epilogue& epi,
+                                const TcSplit& split, unsigned* err, uint64_t limit_ns,
+                                cudaStream_t stream);
+// C (M x N) := the epilogue applied to the sum, in split order, of the
+// partials ws[s * ws_rows + i][j] (row stride ws_ld floats, 16-byte aligned).
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
+                                 float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
+                                 cudaStream_t stream);
 // b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,

@@ -5,6 +5,8 @@
 //               the caller's layout (e.g. K = 777 floats: 3108-byte rows).
 //   fill_zero   C := 0 for K == 0 (the empty sum).
 //   scale       C := beta * C, the generalised product when alpha == 0 or K == 0.
+//   splitk_reduce  adds the K-split partials of the tensor kernel in split
+//               order and applies the epilogue.
 //   wait_selftest  one CTA waits on an mbarrier that nothing completes, to
 //               show the bounded wait gives up and reports instead of hanging.
 #include <cuda_bf16.h>
@@ -167,6 +169,58 @@ __global__ void scale_kernel(float* __restrict__ C, int64_t n, float beta) {
         C[i] = __fmul_rn(beta, C[i]);
 }
 
+// K-split fix-up: C_ij := epilogue(p_0 + p_1 + ... + p_{S-1}), the partials
+// p_s = ws[(s * ws_rows + i) * ws_ld + j] added in split order (the same sum
+// on every run).  Each thread loads four partials before adding them, so
+// several loads are in flight.  Vector form: four columns per thread, for
+// N % 4 == 0 and a 16-byte aligned C (ws rows are always 16-byte aligned).
+template <bool kVec>
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t ws_rows,
+                         int64_t ws_ld, float* __restrict__ C, int64_t M, int64_t N,
+                         const Epilogue epi) {
+    constexpr int W = kVec ? 4 : 1;
+    const int64_t nw = (N + W - 1) / W, units = M * nw;
+    const int64_t sstride = ws_rows * ws_ld;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = u / nw, j = (u - i * nw) * W;
+        const float* p = ws + i * ws_ld + j;
+        if constexpr (kVec) {
+            float4 acc = __ldcg(reinterpret_cast<const float4*>(p));
+            int s = 1;
+            for (; s + 4 <= splits; s += 4) {
+                float4 v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[q] = __ldcg(reinterpret_cast<const float4*>(p + (s + q) * sstride));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc.x += v[q].x, acc.y += v[q].y, acc.z += v[q].z, acc.w += v[q].w;
+            }
+            for (; s < splits; ++s) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p + s * sstride));
+                acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+            }
+            float* c = C + i * N + j;
+            *reinterpret_cast<float4*>(c) = epilogue_apply4(epi, acc, c);
+        } else {
+            float acc = __ldcg(p);
+            int s = 1;
+            for (; s + 4 <= splits; s += 4) {
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = __ldcg(p + (s + q) * sstride);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc += v[q];
+            }
+            for (; s < splits; ++s) acc += __ldcg(p + s * sstride);
+            float* c = C + i * N + j;
+            *c = epilogue_apply(epi, acc, c);
+        }
+    }
+}
+
 __global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -288,6 +342,22 @@ cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
     int64_t blocks = (n + 255) / 256;
     scale_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(C, n, beta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
+                                 float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
+                                 cudaStream_t stream) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (splits < 1 || ws_rows < M || ws_ld < N || ws_ld % 4 != 0) return cudaErrorInvalidValue;
+    const bool vec = c_vec && N % 4 == 0;
+    const int64_t units = M * (vec ? N / 4 : N);
+    const int64_t blocks = (units + 255) / 256;
+    const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
+    if (vec)
+        splitk_reduce_kernel<true><<<grid, 256, 0, stream>>>(ws, splits, ws_rows, ws_ld, C, M, N, epi);
+    else
+        splitk_reduce_kernel<false><<<grid, 256, 0, stream>>>(ws, splits, ws_rows, ws_ld, C, M, N, epi);
     return cudaGetLastError();
 }
 

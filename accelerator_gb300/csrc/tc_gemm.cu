@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_c, float* __restrict__ C, int M,
                         int N, int K, int pairs_m, int tiles_n, int c_mode, const Epilogue epi,
-                        unsigned* err, uint64_t limit_ns) {
+                        int splits, int k_per_split, int ws_rows, unsigned* err,
+                        uint64_t limit_ns) {
     using T = Traits<MODE>;
     constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
     constexpr int kUmmaK = 32 / T::kEs;                   // K per MMA: 16 / 8
@@ -410,6 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npairs = pairs_m * tiles_n;
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     const int nk = (K + kKElems - 1) / kKElems;
+    // Work units: pair tile u / splits over K slabs [kb0, kb1) of split
+    // u % splits.  With splits > 1 the epilogue stores the raw partial sum
+    // into rows split * ws_rows + row of the workspace map_c describes.
+    const int kps = splits > 1 ? k_per_split : nk;
+    const int nunits = npairs * splits;
     // the pair tile p covers rows pm*256 .. +255 and columns pn*256 .. +255
     auto coords = [&](int p, int& m0, int& n0) {
         const int per_group = kGroupM * tiles_n;
@@ -418,6 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gsize = min(pairs_m - first_m, kGroupM);
         m0 = (first_m + (p % per_group) % gsize) * (2 * kBM);
         n0 = ((p % per_group) / gsize) * kBN;
+    };
+    auto unit = [&](int u, int& m0, int& n0, int& kb0, int& kb1, int& split) {
+        const int p = u / splits;
+        split = u - p * splits;
+        coords(p, m0, n0);
+        kb0 = split * kps;
+        kb1 = min(nk, kb0 + kps);
     };
 
     if (warp == 0) {
@@ -431,12 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t last_phase[kPStages];
             bool used[kPStages];
             for (int s = 0; s < kPStages; ++s) used[s] = false, last_phase[s] = 0;
-            for (int p = cluster_id; p < npairs; p += nclusters) {
-                int m0, n0;
-                coords(p, m0, n0);
+            for (int u = cluster_id; u < nunits; u += nclusters) {
+                int m0, n0, kb0, kb1, split;
+                unit(u, m0, n0, kb0, kb1, split);
                 const int my_m0 = m0 + (int)rank * kBM, my_n0 = n0 + (int)rank * kPHalfN;
                 bool ok = true;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, err, limit_ns)) {
                         ok = false;
                         break;
@@ -470,14 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int lt = 0;
-            for (int p = cluster_id; p < npairs; p += nclusters, ++lt) {
+            for (int u = cluster_id; u < nunits; u += nclusters, ++lt) {
+                int m0, n0, kb0, kb1, split;
+                unit(u, m0, n0, kb0, kb1, split);
                 const int buf = lt & 1;
                 const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
                 if (!mbar_wait(acce0 + 8 * buf, use_parity ^ 1u, abort_flag, err, limit_ns)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kAccCols);
                 bool ok = true;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err, limit_ns)) {
                         ok = false;
                         break;
@@ -491,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bdesc =
                             kBKMajor ? smem_desc_sw128(b_tile + kk * 32, 16, 1024)
                                      : smem_desc_sw128(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes, 1024);
-                        tc_mma_pair<T::kKind>(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_pair<T::kKind>(d_tmem, adesc, bdesc, kIdesc,
+                                              (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     tc_commit_pair_multicast(empty0 + 8 * stage, 0x3);   // frees the slot in both CTAs
                     if (++stage == kPStages) stage = 0, phase ^= 1u;
@@ -509,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acce_leader0 = mapa_shared(acce0, 0);
         int stored = 0;   // TMA stores issued by this warp (lane 0's count, shared)
         int lt = 0;
-        for (int p = cluster_id; p < npairs; p += nclusters, ++lt) {
-            int m0, n0;
-            coords(p, m0, n0);
+        for (int u = cluster_id; u < nunits; u += nclusters, ++lt) {
+            int m0, n0, kb0, kb1, split;
+            unit(u, m0, n0, kb0, kb1, split);
             const int buf = lt & 1;
             const uint32_t use_parity = (uint32_t)(lt >> 1) & 1u;
             int ok = 0;
@@ -546,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0 && row0 < M && col0 < N) {
-                        tma_store_2d(&map_c, stg, col0, row0);
+                        tma_store_2d(&map_c, stg, col0, row0 + split * ws_rows);
                         bulk_commit_group();
                         ++stored;
                     }
@@ -647,15 +663,60 @@ cudaError_t tc_setup() {
 
 int tc_max_pairs() { return g_max_pairs; }
 
+// Split count for the pair kernel, from a cost model in units of one K slab
+// of one pair tile (about 0.33 us in either mode: 2*256*256*64 BF16 or
+// 2*256*256*32 TF32 FLOP at 1/76 of the tensor rate):
+//   unsplit   waves(pairs) * (nk + overhead)
+//   S splits  waves(pairs * S) * (ceil(nk / S) + overhead) + reduce launch
+//             + the bytes of S partials written and read and C written, at
+//               about 2 MB per slab time (~6 TB/s)
+// A split must save at least 10 % and keep >= kMinSplitSlabs slabs per unit.
+TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K) {
+    constexpr double kUnitOverhead = 4.0, kReduceFixed = 6.0, kBytesPerSlab = 2.0e6;
+    constexpr int kMinSplitSlabs = 4, kMaxSplits = 128;
+    constexpr double kMaxWorkspace = 512.0 * 1024 * 1024;
+    const int es = mode == TcMode::kTF32 ? 4 : 2;
+    const int64_t kel = kSlabBytes / es;
+    const int64_t nk = (K + kel - 1) / kel;
+    const int64_t pairs = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+    const int64_t clusters = g_max_pairs;
+    if (clusters <= 0 || pairs <= 0 || pairs >= clusters || nk < 2 * kMinSplitSlabs)
+        return kNoSplit;
+    const int64_t ws_rows = (M + 2 * kBM - 1) / (2 * kBM) * (2 * kBM);
+    const int64_t ws_ld = (N + 3) / 4 * 4;
+    const double mn_bytes = 4.0 * (double)M * (double)N;
+    auto waves = [&](int64_t units) { return (double)((units + clusters - 1) / clusters); };
+    double best = waves(pairs) * ((double)nk + kUnitOverhead);
+    TcSplit plan = kNoSplit;
+    for (int64_t S = 2; S <= kMaxSplits && S * kMinSplitSlabs <= nk; ++S) {
+        const int64_t kps = (nk + S - 1) / S;
+        if ((nk + kps - 1) / kps != S) continue;   // every unit must have a slab
+        if ((double)S * ws_rows * ws_ld * 4.0 > kMaxWorkspace) break;
+        const double cost = waves(pairs * S) * ((double)kps + kUnitOverhead) + kReduceFixed +
+                            (2.0 * S + 1.0) * mn_bytes / kBytesPerSlab;
+        if (cost < 0.9 * best) {
+            best = cost;
+            plan = TcSplit{(int)S, (int)kps, (int)ws_rows};
+        }
+    }
+    return plan;
+}
+
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, const Epilogue& epi, unsigned* err,
-                                uint64_t limit_ns, cudaStream_t stream) {
+                                int N, int K, bool c_vec, const Epilogue& epi,
+                                const TcSplit& split, unsigned* err, uint64_t limit_ns,
+                                cudaStream_t stream) {
     const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
     const int64_t pairs = (int64_t)pairs_m * tiles_n;
     if (pairs <= 0) return cudaSuccess;
     if (pairs > 0x3FFFFFFF || g_max_pairs <= 0) return cudaErrorInvalidValue;
-    const int clusters = (int)(pairs < g_max_pairs ? pairs : g_max_pairs);
+    // K splits write raw partials through the TMA store into the workspace
+    if (split.splits > 1 && (!map_c || epi.kind != 0 || split.ws_rows % (2 * kBM) != 0))
+        return cudaErrorInvalidValue;
+    const int64_t units = pairs * (split.splits > 1 ? split.splits : 1);
+    if (units > 0x3FFFFFFF) return cudaErrorInvalidValue;
+    const int clusters = (int)(units < g_max_pairs ? units : g_max_pairs);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters));
     cfg.blockDim = dim3(kThreads);
@@ -670,16 +731,18 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     cfg.numAttrs = 1;
     const int cm = map_c ? kStoreTma : (c_vec ? kStoreVec : kStoreScalar);
     const CUtensorMap& mc = map_c ? *map_c : map_a;   // unused unless cm == kStoreTma
+    const int sp = split.splits > 1 ? split.splits : 1;
+    const int kps = sp > 1 ? split.k_per_split : 0, wr = sp > 1 ? split.ws_rows : 0;
     cudaError_t e;
     if (mode == TcMode::kBF16 && !b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
     else if (mode == TcMode::kTF32 && b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
     else if (mode == TcMode::kF16 && !b_k_major)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, err, limit_ns);
+                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
     else
         return cudaErrorInvalidValue;
     return e != cudaSuccess ? e : cudaGetLastError();
