@@ -118,7 +118,7 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
     void* scratch = nullptr;
     float* partial = nullptr;
     unsigned* counters = nullptr;
-    if (plan.split_tiles > 0) {
+    if (plan.split_tiles > 0 && !plan.wide) {
         const int64_t pb = round_up(plan.partial_bytes, 256), cb = round_up(plan.counter_bytes, 256);
         if (cudaMallocFromPoolAsync(&scratch, (size_t)(pb + cb), st->pool, stream) != cudaSuccess) {
             cudaGetLastError();
@@ -133,12 +133,27 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
         }
         g_launches++;
     }
+    float* ws = nullptr;
+    if (plan.wide) {
+        if (cudaMallocFromPoolAsync(&scratch, (size_t)round_up(plan.ws_bytes, 256), st->pool,
+                                    stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NO_MEMORY;
+        }
+        ws = static_cast<float*>(scratch);
+    }
     int rc = GEMM_OK;
     if (launch_ffma_sgemm(A, B, C, (int)M, (int)N, (int)K, b_vec, c_vec, plan, partial, counters,
-                          epi, stream) != cudaSuccess)
+                          epi, ws, stream) != cudaSuccess)
         rc = GEMM_ERR_CUDA;
     else
         g_launches++;
+    if (rc == GEMM_OK && plan.wide) {
+        if (launch_splitk_reduce(ws, plan.splits, M, N, C, M, N, c_vec, epi, stream) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        else
+            g_launches++;
+    }
     if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }

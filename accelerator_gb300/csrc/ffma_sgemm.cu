@@ -179,7 +179,7 @@ struct SlabLoader {
 // such CTA writes its partial tile to `partial`, and the last of them to
 // finish (an atomic counter per tile) adds the partials in split order and
 // stores C.  The sum is then ((p0 + p1) + p2) + ..., the same on every run.
-template <class CF, bool kBVec, bool kCVec>
+template <class CF, bool kBVec, bool kCVec, bool kWide>
 __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     ffma_sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                       float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
@@ -289,7 +289,12 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     }
     cp_async_wait<0>();
 
-    if ((int)blockIdx.x >= dp_tiles) {
+    if constexpr (kWide) {
+        // Wide split (every CTA a piece): `partial` is a workspace of
+        // `splits` M x N blocks; store this K range's raw partial into block
+        // `part` as if it were C (a separate kernel adds the blocks in order).
+        C = partial + (int64_t)part * M * N;
+    } else if ((int)blockIdx.x >= dp_tiles) {
         // Split tile: publish this K range's partial, then let the last CTA
         // of the tile combine all of them.
         const int st = tile - dp_tiles;
@@ -349,7 +354,11 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
 
 template <bool BV, bool CV>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV>,
+    cudaError_t e = cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)FfmaCfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)FfmaCfg::kSmemBytes);
 }
@@ -365,7 +374,7 @@ cudaError_t ffma_setup() {
     if ((e = set_smem_attr<true, false>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<true, true>()) != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffma_sgemm_kernel<FfmaCfg, true, true>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffma_sgemm_kernel<FfmaCfg, true, true, false>,
                                                       FfmaCfg::kThreads, FfmaCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     g_ctas_per_sm = n > 0 ? n : 1;
@@ -382,6 +391,27 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
     p.dp_tiles = tiles;
     p.splits = 1;
     const int64_t rem = slots > 0 ? tiles % slots : 0;
+    // Few tiles and a long K: more pieces than the in-kernel combination
+    // handles well.  Every tile is split (at least kMinSlabs slabs a piece,
+    // one wave, at most 256 pieces and kMaxWorkspace bytes of partials), each
+    // piece stores its partial as a whole M x N block, and a second kernel
+    // adds the blocks in piece order.
+    constexpr int64_t kMinSlabsWide = 4, kMaxWorkspace = 512ll << 20;
+    if (slots > 0 && tiles < slots && slots / tiles > 16 && nkt / kMinSlabsWide > 16) {
+        int64_t s = slots / tiles;
+        if (s > nkt / kMinSlabsWide) s = nkt / kMinSlabsWide;
+        if (s > 256) s = 256;
+        const int64_t block = (int64_t)M * N * (int64_t)sizeof(float);
+        if (s * block > kMaxWorkspace) s = kMaxWorkspace / block;
+        if (s > 16) {
+            p.splits = (int)s;
+            p.dp_tiles = 0;
+            p.split_tiles = tiles;
+            p.wide = true;
+            p.ws_bytes = s * block;
+            return p;
+        }
+    }
     // Split the tiles of a partial last wave along K, as many ways as still
     // fit in one wave, keeping at least kMinSlabs slabs per piece.
     constexpr int64_t kMinSlabs = 8;
@@ -400,24 +430,45 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
     return p;
 }
 
+// Launches the variant for the operands' vector widths; the wide split has
+// its own instantiation so that the other kernels compile as they would
+// without it.
+template <bool BV, bool CV>
+static void launch_variant(dim3 grid, size_t smem, cudaStream_t stream, const float* A,
+                           const float* B, float* C, int M, int N, int K, int tiles_m,
+                           int tiles_n, int dp, int sp, const FfmaPlan& plan, float* partial,
+                           unsigned* counters, float* ws, const Epilogue& epi) {
+    if (plan.wide)
+        ffma_sgemm_kernel<FfmaCfg, BV, CV, true><<<grid, FfmaCfg::kThreads, smem, stream>>>(
+            A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, ws, nullptr, kPlainStore);
+    else
+        ffma_sgemm_kernel<FfmaCfg, BV, CV, false><<<grid, FfmaCfg::kThreads, smem, stream>>>(
+            A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters, epi);
+}
+
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
                               bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, const Epilogue& epi, cudaStream_t stream) {
+                              unsigned* counters, const Epilogue& epi, float* ws,
+                              cudaStream_t stream) {
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     if (plan.tiles <= 0) return cudaSuccess;
     const int64_t ctas = plan.dp_tiles + plan.split_tiles * plan.splits;
-    if (ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    dim3 grid((unsigned)ctas), block(FfmaCfg::kThreads);
+    if (ctas > 0x7FFFFFFF || (plan.wide && !ws)) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)ctas);
     const int dp = (int)plan.dp_tiles, sp = plan.splits;
     const size_t smem = FfmaCfg::kSmemBytes;
-#define LIBGEMM_FFMA_LAUNCH(BV, CV)                                                            \
-    ffma_sgemm_kernel<FfmaCfg, BV, CV><<<grid, block, smem, stream>>>(                         \
-        A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters, epi)
-    if (b_vec && c_vec) LIBGEMM_FFMA_LAUNCH(true, true);
-    else if (b_vec) LIBGEMM_FFMA_LAUNCH(true, false);
-    else if (c_vec) LIBGEMM_FFMA_LAUNCH(false, true);
-    else LIBGEMM_FFMA_LAUNCH(false, false);
-#undef LIBGEMM_FFMA_LAUNCH
+    if (b_vec && c_vec)
+        launch_variant<true, true>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+                                   plan, partial, counters, ws, epi);
+    else if (b_vec)
+        launch_variant<true, false>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+                                    plan, partial, counters, ws, epi);
+    else if (c_vec)
+        launch_variant<false, true>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+                                    plan, partial, counters, ws, epi);
+    else
+        launch_variant<false, false>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp,
+                                     sp, plan, partial, counters, ws, epi);
     return cudaGetLastError();
 }
 

@@ -46,16 +46,22 @@ __device__ __forceinline__ float4 epilogue_apply4(const Epilogue& e, float4 acc,
 // Work split: the first dp_tiles tiles whole, the last split_tiles tiles each
 // in `splits` K ranges whose partials (partial_bytes of scratch) are summed by
 // the last CTA of the tile (counter_bytes of zeroed counters).
+// Wide plan (wide = true): every tile is split; the pieces store their raw
+// partials into ws_bytes of workspace (splits blocks of M x N floats) and
+// launch_splitk_reduce adds them and applies the epilogue.
 struct FfmaPlan {
     int64_t tiles, dp_tiles, split_tiles;
     int splits;
     int64_t partial_bytes, counter_bytes;
+    bool wide;
+    int64_t ws_bytes;
 };
 cudaError_t ffma_setup();
 FfmaPlan ffma_plan(int M, int N, int K, int num_sms);
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
                               bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, const Epilogue& epi, cudaStream_t stream);
+                              unsigned* counters, const Epilogue& epi, float* ws,
+                              cudaStream_t stream);
 
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
 enum class TcMode { kBF16, kTF32, kF16 };
@@ -90,7 +96,7 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
                                 const TcSplit& split, unsigned* err, uint64_t limit_ns,
                                 cudaStream_t stream);
 // C (M x N) := the epilogue applied to the sum, in split order, of the
-// partials ws[s * ws_rows + i][j] (row stride ws_ld floats, 16-byte aligned).
+// partials ws[s * ws_rows + i][j] (row stride ws_ld floats).
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
                                  float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
                                  cudaStream_t stream);

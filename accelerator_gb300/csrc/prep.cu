@@ -173,7 +173,7 @@ __global__ void scale_kernel(float* __restrict__ C, int64_t n, float beta) {
 // p_s = ws[(s * ws_rows + i) * ws_ld + j] added in split order (the same sum
 // on every run).  Each thread loads four partials before adding them, so
 // several loads are in flight.  Vector form: four columns per thread, for
-// N % 4 == 0 and a 16-byte aligned C (ws rows are always 16-byte aligned).
+// N % 4 == 0 and 16-byte aligned rows of C and of ws.
 template <bool kVec>
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t ws_rows,
@@ -349,8 +349,9 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, i
                                  float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
                                  cudaStream_t stream) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    if (splits < 1 || ws_rows < M || ws_ld < N || ws_ld % 4 != 0) return cudaErrorInvalidValue;
-    const bool vec = c_vec && N % 4 == 0;
+    if (splits < 1 || ws_rows < M || ws_ld < N) return cudaErrorInvalidValue;
+    const bool vec = c_vec && N % 4 == 0 && ws_ld % 4 == 0 &&
+                     (reinterpret_cast<uintptr_t>(ws) & 15u) == 0;
     const int64_t units = M * (vec ? N / 4 : N);
     const int64_t blocks = (units + 255) / 256;
     const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);

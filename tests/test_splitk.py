@@ -6,7 +6,10 @@ adds in a fixed order in a second kernel, which also applies the update of
 gemm_ex.  Covered here: square-ish small-MN/large-K shapes, a single-tile
 shape split dozens of ways, ragged M, N and K (a partial last K slab, N not
 a multiple of 4: the element-wise fix-up), run-to-run determinism, and that
-the split really is taken (two kernels for an aligned BF16 product).
+the split really is taken (two kernels for an aligned BF16 product).  The
+FP32 (FFMA) path splits shapes with very few tiles the same way ("wide"
+split: every tile cut into up to 256 K ranges, partials added by the same
+second kernel); it is covered by the same checks.
 """
 import numpy as np
 import pytest
@@ -40,8 +43,13 @@ def test_small_mn_large_k(libgemm, mode, M, K, N):
     _sampled(libgemm, M, K, N, mode)
 
 
-@pytest.mark.parametrize("mode", TC_MODES + ["fp32_via_bf16"])
-@pytest.mark.parametrize("M,K,N", [(300, 9001, 203), (257, 4100, 130)])
+@pytest.mark.parametrize("M,K,N", [(256, 65536, 256), (128, 8192, 128)])
+def test_fp32_wide_split(libgemm, M, K, N):
+    _sampled(libgemm, M, K, N, "fp32")
+
+
+@pytest.mark.parametrize("mode", TC_MODES + ["fp32_via_bf16", "fp32"])
+@pytest.mark.parametrize("M,K,N", [(300, 9001, 203), (257, 4100, 130), (100, 5000, 77)])
 def test_ragged_split_full(libgemm, mode, M, K, N):
     A, B = inputs.matrices(M, K, N, "pm1", seed=M * 3 + N)
     C = run(libgemm, A, B, mode)
@@ -53,7 +61,7 @@ def test_ragged_split_full(libgemm, mode, M, K, N):
     assert_within(C, Cref, S, TOL[mode], f"{mode} {M}x{K}x{N}")
 
 
-@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("mode", ["bf16", "tf32", "fp32"])
 def test_integers_bit_exact_when_split(libgemm, mode):
     # |C| <= 16 * 8192 < 2**24 and every partial is an integer: exact in any order
     A, B = inputs.matrices(192, 8192, 320, "int4", seed=4)
@@ -62,9 +70,10 @@ def test_integers_bit_exact_when_split(libgemm, mode):
     np.testing.assert_array_equal(C.astype(np.float64), Cref)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("mode", ["bf16", "tf32", "fp32"])
 def test_split_is_deterministic(libgemm, mode):
-    A, B = inputs.matrices(512, 12288, 384, "pm1", seed=9)
+    A, B = inputs.matrices(512, 12288, 384, "pm1", seed=9) if mode != "fp32" else \
+        inputs.matrices(128, 12288, 256, "pm1", seed=9)
     first = run(libgemm, A, B, mode)
     for _ in range(2):
         np.testing.assert_array_equal(run(libgemm, A, B, mode), first)
@@ -86,9 +95,14 @@ def test_split_is_taken(libgemm):
     libgemm.gemm(a2, b2, c2, mode=libgemm.BF16)   # 256 tiles fill the GPU: no split
     torch.cuda.synchronize()
     assert libgemm.launch_count() - n1 == 1
+    a3, b3 = device_operands(A, B, "fp32")
+    n2 = libgemm.launch_count()
+    libgemm.gemm(a3, b3, c, mode=libgemm.FP32)    # 4 FFMA tiles: wide split + fix-up kernel
+    torch.cuda.synchronize()
+    assert libgemm.launch_count() - n2 == 2
 
 
-@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("mode", ["bf16", "tf32", "fp32"])
 @pytest.mark.parametrize("N", [256, 203])
 def test_split_with_update(libgemm, mode, N):
     """gemm_ex on a split product: the update is applied once, after the sum."""
