@@ -164,34 +164,34 @@ CUtensorMapDataType tensor_type(TcMode mode) {
                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// K-split product: the pair kernel writes split.splits raw partials into a
-// workspace from the pool (split.ws_rows rows each, row stride N rounded up
-// to 4 floats), then the reduce kernel adds them in split order, applies the
-// epilogue and writes C.
+// K-split product: the pair kernel computes the whole tiles into C (with
+// the epilogue) and stores the split units' raw partials as 256 x 256 blocks
+// of a workspace from the pool; the reduce kernel adds each split tile's
+// blocks in split order, applies the epilogue and writes C.
 int split_tc_launch(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
-                    const CUtensorMap& map_b, float* C, int64_t M, int64_t K, int64_t N,
-                    bool c_vec, const Epilogue& epi, const TcSplit& split, DeviceState* st,
-                    cudaStream_t stream) {
-    const int64_t ws_ld = round_up(N, 4), ws_rows_all = (int64_t)split.splits * split.ws_rows;
+                    const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int64_t M,
+                    int64_t K, int64_t N, bool c_vec, const Epilogue& epi, const TcSplit& split,
+                    DeviceState* st, cudaStream_t stream) {
+    const int64_t bytes = tc_split_workspace_bytes(split, M, N);
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, (size_t)(ws_rows_all * ws_ld * 4), st->pool, stream) !=
-        cudaSuccess) {
+    if (cudaMallocFromPoolAsync(&ws, (size_t)bytes, st->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_NO_MEMORY;
     }
     CUtensorMap map_w;
-    int rc = encode_2d(&map_w, ws, 4, ws_rows_all, N, ws_ld, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    int rc = encode_2d(&map_w, ws, 4, bytes / (256 * 4), 256, 256, 32, 32,
+                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
     if (rc == GEMM_OK) {
-        if (launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, &map_w, static_cast<float*>(ws),
-                                (int)M, (int)N, (int)K, true, kPlainStore, split, st->err,
-                                kWaitLimitNs, stream) != cudaSuccess)
+        if (launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, map_c, &map_w, C, (int)M, (int)N,
+                                (int)K, c_vec, epi, split, st->err, kWaitLimitNs, stream) !=
+            cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
             g_launches++;
     }
     if (rc == GEMM_OK) {
-        if (launch_splitk_reduce(static_cast<const float*>(ws), split.splits, split.ws_rows, ws_ld,
-                                 C, M, N, c_vec, epi, stream) != cudaSuccess)
+        if (launch_tc_tile_reduce(static_cast<const float*>(ws), split, C, (int)M, (int)N, c_vec,
+                                  epi, stream) != cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
             g_launches++;
@@ -225,13 +225,13 @@ int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const
                        encode_2d(&map_c, C, 4, M, N, N, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) == GEMM_OK;
     const TcSplit split = pairs && rc == GEMM_OK ? tc_plan_split(mode, M, N, K) : kNoSplit;
     if (rc == GEMM_OK && split.splits > 1)
-        return split_tc_launch(mode, b_k_major, map_a, map_b, C, M, K, N, c_vec, epi, split, st,
-                               stream);
+        return split_tc_launch(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C, M, K, N,
+                               c_vec, epi, split, st, stream);
     if (rc == GEMM_OK) {
         const cudaError_t e =
-            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C,
-                                        (int)M, (int)N, (int)K, c_vec, epi, kNoSplit, st->err,
-                                        kWaitLimitNs, stream)
+            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr,
+                                        nullptr, C, (int)M, (int)N, (int)K, c_vec, epi, kNoSplit,
+                                        st->err, kWaitLimitNs, stream)
                   : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
                                    epi, st->num_sms, st->err, kWaitLimitNs, stream);
         if (e != cudaSuccess)

@@ -79,22 +79,32 @@ int tc_max_pairs();
 // bytes (MN-major) or 128 rows x 128 bytes (K-major), i.e. block_n / 2 wide.
 // map_c (may be null): C as a 2-D fp32 tensor, box 32 x 32, 128-byte swizzle,
 // for TMA stores of the epilogue; without it C is stored by the threads.
-// K split of the pair kernel: splits units per pair tile, each over
-// k_per_split K slabs (k_elems each; the last unit takes the rest, and every
-// unit has at least one), storing raw partials through map_c into a
-// workspace of splits blocks of ws_rows rows (ws_rows a multiple of 256).
+// K split of the pair kernel: the first whole_tiles pair tiles (in the
+// kernel's raster order) are computed whole into C; every later tile as
+// `splits` units of k_per_split K slabs (k_elems each; the last unit takes
+// the rest, and every unit has at least one), each storing its raw partial
+// as one 256 x 256 fp32 block of a workspace (block (tile - whole_tiles) *
+// splits + split), which launch_tc_tile_reduce adds up into C.
 struct TcSplit {
-    int splits, k_per_split, ws_rows;
+    int splits, k_per_split, whole_tiles;
 };
 constexpr TcSplit kNoSplit{1, 0, 0};
 // The split the pair kernel should use for an M x K x N product (kNoSplit
-// when the tiles alone fill the GPU, or splitting would not pay).
+// when splitting would not pay).
 TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K);
+// Workspace bytes a split needs (0 for kNoSplit).
+int64_t tc_split_workspace_bytes(const TcSplit& split, int64_t M, int64_t N);
+// map_w (needed when split.splits > 1): the workspace as a 2-D fp32 tensor of
+// 256 columns, row stride 256, box 32 x 32, 128-byte swizzle.
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
-                                const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, const Epilogue& epi,
-                                const TcSplit& split, unsigned* err, uint64_t limit_ns,
-                                cudaStream_t stream);
+                                const CUtensorMap& map_b, const CUtensorMap* map_c,
+                                const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
+                                const Epilogue& epi, const TcSplit& split, unsigned* err,
+                                uint64_t limit_ns, cudaStream_t stream);
+// C := the epilogue applied to the sum, in split order, of the workspace
+// blocks of every split tile (the whole tiles are left as they are).
+cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* C, int M, int N,
+                                  bool c_vec, const Epilogue& epi, cudaStream_t stream);
 // C (M x N) := the epilogue applied to the sum, in split order, of the
 // partials ws[s * ws_rows + i][j] (row stride ws_ld floats).
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,

@@ -131,9 +131,9 @@ extern "C" int gemm_tf32_noalloc(const float* A, const float* B, float* C, int64
     const bool c_tma =
         pairs && c_vec && encode_tensor_map_2d(&map_c, C, 4, M, N, N, 32, 32) == GEMM_OK;
     const cudaError_t e =
-        pairs ? launch_tc_gemm_pair(TcMode::kTF32, true, map_a, map_b, c_tma ? &map_c : nullptr, C,
-                                    (int)M, (int)N, (int)K, c_vec, kPlainStore, kNoSplit, err, kWaitLimitNs,
-                                    stream)
+        pairs ? launch_tc_gemm_pair(TcMode::kTF32, true, map_a, map_b, c_tma ? &map_c : nullptr,
+                                    nullptr, C, (int)M, (int)N, (int)K, c_vec, kPlainStore, kNoSplit,
+                                    err, kWaitLimitNs, stream)
               : launch_tc_gemm(TcMode::kTF32, true, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
                                kPlainStore, num_sms, err, kWaitLimitNs, stream);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;

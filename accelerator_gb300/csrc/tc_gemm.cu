@@ -337,6 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warps 2-5  epilogue of this CTA's rows; each warp then arrives on the
 //           leader's accumulator-empty barrier (count 8: 4 warps x 2 CTAs).
 constexpr int kPStages = 6;
+
+// Pair tile p of the pair kernel's grouped raster: rows m0 .. m0 + 255,
+// columns n0 .. n0 + 255 (consecutive tiles walk down kGroupM tile rows).
+__device__ __forceinline__ void pair_coords(int p, int pairs_m, int tiles_n, int& m0, int& n0) {
+    const int per_group = kGroupM * tiles_n;
+    const int group = p / per_group;
+    const int first_m = group * kGroupM;
+    const int gsize = min(pairs_m - first_m, kGroupM);
+    m0 = (first_m + (p % per_group) % gsize) * (2 * kBM);
+    n0 = ((p % per_group) / gsize) * kBN;
+}
 // How the pair kernel writes C: TMA stores from swizzled staging (16-byte
 // aligned C rows), 16-byte vector stores, or 4-byte stores.
 enum : int { kStoreScalar = 0, kStoreVec = 1, kStoreTma = 2 };
@@ -354,9 +365,10 @@ template <TcMode MODE, bool kBKMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
-                        const __grid_constant__ CUtensorMap map_c, float* __restrict__ C, int M,
+                        const __grid_constant__ CUtensorMap map_c,
+                        const __grid_constant__ CUtensorMap map_w, float* __restrict__ C, int M,
                         int N, int K, int pairs_m, int tiles_n, int c_mode, const Epilogue epi,
-                        int splits, int k_per_split, int ws_rows, unsigned* err,
+                        int splits, int k_per_split, int whole_tiles, unsigned* err,
                         uint64_t limit_ns) {
     using T = Traits<MODE>;
     constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
@@ -411,26 +423,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npairs = pairs_m * tiles_n;
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     const int nk = (K + kKElems - 1) / kKElems;
-    // Work units: pair tile u / splits over K slabs [kb0, kb1) of split
-    // u % splits.  With splits > 1 the epilogue stores the raw partial sum
-    // into rows split * ws_rows + row of the workspace map_c describes.
+    // Work units: the first whole_tiles pair tiles whole (unit u is tile u,
+    // all K), then each remaining tile as `splits` units over K slabs
+    // [kb0, kb1).  A split unit stores its raw partial sum as one 256 x 256
+    // block of the workspace map_w describes: block (tile - whole_tiles) *
+    // splits + split, rows block * 256 .. +255.
     const int kps = splits > 1 ? k_per_split : nk;
-    const int nunits = npairs * splits;
+    const int nunits = whole_tiles + (npairs - whole_tiles) * splits;
     // the pair tile p covers rows pm*256 .. +255 and columns pn*256 .. +255
-    auto coords = [&](int p, int& m0, int& n0) {
-        const int per_group = kGroupM * tiles_n;
-        const int group = p / per_group;
-        const int first_m = group * kGroupM;
-        const int gsize = min(pairs_m - first_m, kGroupM);
-        m0 = (first_m + (p % per_group) % gsize) * (2 * kBM);
-        n0 = ((p % per_group) / gsize) * kBN;
-    };
+    auto coords = [&](int p, int& m0, int& n0) { pair_coords(p, pairs_m, tiles_n, m0, n0); };
+    // split = -1: a whole tile (stored to C); otherwise the workspace block
     auto unit = [&](int u, int& m0, int& n0, int& kb0, int& kb1, int& split) {
-        const int p = u / splits;
-        split = u - p * splits;
-        coords(p, m0, n0);
-        kb0 = split * kps;
+        if (u < whole_tiles) {
+            coords(u, m0, n0);
+            kb0 = 0, kb1 = nk, split = -1;
+            return;
+        }
+        const int v = u - whole_tiles, t = v / splits;
+        coords(whole_tiles + t, m0, n0);
+        kb0 = (v - t * splits) * kps;
         kb1 = min(nk, kb0 + kps);
+        split = v;   // workspace block index
     };
 
     if (warp == 0) {
@@ -539,14 +552,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = row0 + lane;
             float* crow = C + (int64_t)row * N;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kAccCols);
+            // a split unit stores raw partials, always through TMA, into its block
+            const bool to_ws = split >= 0;
+            const int mode_u = to_ws ? kStoreTma : c_mode;
+            const int ws_row0 = split * (2 * kBM) + (int)rank * kBM + quarter * 32;
 #pragma unroll 1
             for (int c = 0; c < kAccCols / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
-                epilogue_row32(epi, v, crow, row, col0, M, N, c_mode != kStoreScalar);
-                if (c_mode == kStoreTma) {
+                if (!to_ws) epilogue_row32(epi, v, crow, row, col0, M, N, c_mode != kStoreScalar);
+                if (mode_u == kStoreTma) {
                     // Stage the warp's 32 x 32 block (row = lane) with the 128-byte
                     // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then
                     // one lane writes it with a TMA store that clips at M and N.
@@ -562,13 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0 && row0 < M && col0 < N) {
-                        tma_store_2d(&map_c, stg, col0, row0 + split * ws_rows);
+                        if (to_ws)
+                            tma_store_2d(&map_w, stg, c * 32, ws_row0);
+                        else
+                            tma_store_2d(&map_c, stg, col0, row0);
                         bulk_commit_group();
                         ++stored;
                     }
                     stored = __shfl_sync(0xffffffffu, stored, 0);
                 } else if (row < M) {
-                    if (c_mode == kStoreVec && col0 + 32 <= N) {
+                    if (mode_u == kStoreVec && col0 + 32 <= N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<float4*>(crow + col0 + j) =
@@ -596,6 +616,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+// K-split fix-up of the pair kernel: for each split tile t (pair tiles
+// whole_tiles + t), C := epilogue(sum of workspace blocks t * splits + s,
+// s = 0 .. splits - 1, added in that order: the same sum on every run).  A
+// thread handles four columns of one row; four blocks' loads are issued
+// before they are added.
+__global__ void __launch_bounds__(256)
+    tile_reduce_kernel(const float* __restrict__ ws, int splits, int whole_tiles, int split_tiles,
+                       int pairs_m, int tiles_n, float* __restrict__ C, int M, int N, int c_vec,
+                       const Epilogue epi) {
+    constexpr int kTile = 2 * kBM;                        // 256 x 256 blocks
+    constexpr int64_t kPerTile = (int64_t)kTile * (kTile / 4);
+    constexpr int64_t kBlock = (int64_t)kTile * kTile;
+    const int64_t units = (int64_t)split_tiles * kPerTile;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(u / kPerTile);
+        const int r = (int)((u % kPerTile) / (kTile / 4)), c4 = (int)(u % (kTile / 4));
+        int m0, n0;
+        pair_coords(whole_tiles + t, pairs_m, tiles_n, m0, n0);
+        const int i = m0 + r, j = n0 + 4 * c4;
+        if (i >= M || j >= N) continue;
+        const float* p = ws + ((int64_t)t * splits * kTile + r) * kTile + 4 * c4;
+        float4 acc = __ldcg(reinterpret_cast<const float4*>(p));
+        int sp = 1;
+        for (; sp + 4 <= splits; sp += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[q] = __ldcg(reinterpret_cast<const float4*>(p + (sp + q) * kBlock));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc.x += v[q].x, acc.y += v[q].y, acc.z += v[q].z, acc.w += v[q].w;
+        }
+        for (; sp < splits; ++sp) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p + sp * kBlock));
+            acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+        }
+        float* c = C + (int64_t)i * N + j;
+        if (c_vec) {   // N % 4 == 0: the four columns are inside C
+            *reinterpret_cast<float4*>(c) = epilogue_apply4(epi, acc, c);
+        } else {
+            const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j + q < N) c[q] = epilogue_apply(epi, a[q], c + q);
+        }
     }
 }
 
@@ -663,16 +732,23 @@ cudaError_t tc_setup() {
 
 int tc_max_pairs() { return g_max_pairs; }
 
-// Split count for the pair kernel, from a cost model in units of one K slab
-// of one pair tile (about 0.33 us in either mode: 2*256*256*64 BF16 or
-// 2*256*256*32 TF32 FLOP at 1/76 of the tensor rate):
-//   unsplit   waves(pairs) * (nk + overhead)
-//   S splits  waves(pairs * S) * (ceil(nk / S) + overhead) + reduce launch
-//             + the bytes of S partials written and read and C written, at
-//               about 2 MB per slab time (~6 TB/s)
-// A split must save at least 10 % and keep >= kMinSplitSlabs slabs per unit.
+// K split of the pair kernel, from a cost model in units of one K slab of one
+// pair tile (about 0.33 us in either mode: 2*256*256*64 BF16 or 2*256*256*32
+// TF32 FLOP at 1/76 of the tensor rate), with R = rounds of clusters:
+//   unsplit     R(pairs) * (nk + overhead)
+//   all split   R(pairs * S) * (ceil(nk / S) + overhead) + reduce
+//   tail split  the tiles of a partial last round cut S ways so that they
+//               fill one round: R(whole) * (nk + overhead) + ceil(nk / S) +
+//               overhead + reduce
+// where reduce = a launch plus the workspace blocks (256 KB per tile and
+// split) written and read and C written, at about 2 MB per slab time
+// (~6 TB/s), or 4 MB when the workspace is small enough to stay in L2.
+// A split must save 1 - kMinGain and keep >= kMinSplitSlabs slabs a unit.
+// (Measured at 4096^3 and 8192^3, the tail split gains 1-2 %: less than the
+// model says, since a partly filled last round runs faster per cluster.)
 TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K) {
-    constexpr double kUnitOverhead = 4.0, kReduceFixed = 6.0, kBytesPerSlab = 2.0e6;
+    constexpr double kUnitOverhead = 4.0, kReduceFixed = 6.0, kL2Bytes = 96.0e6;
+    constexpr double kMinGain = 0.98, kBlockBytes = 256.0 * 256.0 * 4.0;
     constexpr int kMinSplitSlabs = 4, kMaxSplits = 128;
     constexpr double kMaxWorkspace = 512.0 * 1024 * 1024;
     const int es = mode == TcMode::kTF32 ? 4 : 2;
@@ -680,41 +756,50 @@ TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K) {
     const int64_t nk = (K + kel - 1) / kel;
     const int64_t pairs = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
     const int64_t clusters = g_max_pairs;
-    if (clusters <= 0 || pairs <= 0 || pairs >= clusters || nk < 2 * kMinSplitSlabs)
-        return kNoSplit;
-    const int64_t ws_rows = (M + 2 * kBM - 1) / (2 * kBM) * (2 * kBM);
-    const int64_t ws_ld = (N + 3) / 4 * 4;
-    const double mn_bytes = 4.0 * (double)M * (double)N;
-    auto waves = [&](int64_t units) { return (double)((units + clusters - 1) / clusters); };
-    double best = waves(pairs) * ((double)nk + kUnitOverhead);
+    if (clusters <= 0 || pairs <= 0 || nk < 2 * kMinSplitSlabs) return kNoSplit;
+    auto rounds = [&](int64_t units) { return (double)((units + clusters - 1) / clusters); };
+    auto reduce = [&](int64_t tiles, int64_t S) {
+        const double ws = (double)tiles * S * kBlockBytes;
+        const double per_slab = ws <= kL2Bytes ? 4.0e6 : 2.0e6;
+        return kReduceFixed + (double)tiles * (2.0 * S + 1.0) * kBlockBytes / per_slab;
+    };
+    const double unsplit = rounds(pairs) * ((double)nk + kUnitOverhead);
+    double best = kMinGain * unsplit;
     TcSplit plan = kNoSplit;
+    const int64_t rem = pairs % clusters, whole = pairs - rem;
     for (int64_t S = 2; S <= kMaxSplits && S * kMinSplitSlabs <= nk; ++S) {
         const int64_t kps = (nk + S - 1) / S;
         if ((nk + kps - 1) / kps != S) continue;   // every unit must have a slab
-        if ((double)S * ws_rows * ws_ld * 4.0 > kMaxWorkspace) break;
-        const double cost = waves(pairs * S) * ((double)kps + kUnitOverhead) + kReduceFixed +
-                            (2.0 * S + 1.0) * mn_bytes / kBytesPerSlab;
-        if (cost < 0.9 * best) {
-            best = cost;
-            plan = TcSplit{(int)S, (int)kps, (int)ws_rows};
+        if (pairs < clusters) {                     // all tiles split
+            if ((double)pairs * S * kBlockBytes > kMaxWorkspace) break;
+            const double cost = rounds(pairs * S) * ((double)kps + kUnitOverhead) + reduce(pairs, S);
+            if (cost < best) best = cost, plan = TcSplit{(int)S, (int)kps, 0};
+        } else if (rem > 0 && rem * S <= clusters) {   // the last round's tiles split
+            if ((double)rem * S * kBlockBytes > kMaxWorkspace) break;
+            const double cost = rounds(whole) * ((double)nk + kUnitOverhead) +
+                                ((double)kps + kUnitOverhead) + reduce(rem, S);
+            if (cost < best) best = cost, plan = TcSplit{(int)S, (int)kps, (int)whole};
         }
     }
     return plan;
 }
 
 cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
-                                const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int M,
-                                int N, int K, bool c_vec, const Epilogue& epi,
-                                const TcSplit& split, unsigned* err, uint64_t limit_ns,
-                                cudaStream_t stream) {
+                                const CUtensorMap& map_b, const CUtensorMap* map_c,
+                                const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
+                                const Epilogue& epi, const TcSplit& split, unsigned* err,
+                                uint64_t limit_ns, cudaStream_t stream) {
     const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
     const int64_t pairs = (int64_t)pairs_m * tiles_n;
     if (pairs <= 0) return cudaSuccess;
     if (pairs > 0x3FFFFFFF || g_max_pairs <= 0) return cudaErrorInvalidValue;
-    // K splits write raw partials through the TMA store into the workspace
-    if (split.splits > 1 && (!map_c || epi.kind != 0 || split.ws_rows % (2 * kBM) != 0))
+    const bool splitting = split.splits > 1;
+    const int sp = splitting ? split.splits : 1;
+    const int64_t whole = splitting ? split.whole_tiles : pairs;
+    // split units store raw partials through TMA into the workspace map_w
+    if (splitting && (!map_w || whole < 0 || whole >= pairs || split.k_per_split < 1))
         return cudaErrorInvalidValue;
-    const int64_t units = pairs * (split.splits > 1 ? split.splits : 1);
+    const int64_t units = whole + (pairs - whole) * sp;
     if (units > 0x3FFFFFFF) return cudaErrorInvalidValue;
     const int clusters = (int)(units < g_max_pairs ? units : g_max_pairs);
     cudaLaunchConfig_t cfg = {};
@@ -731,21 +816,42 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     cfg.numAttrs = 1;
     const int cm = map_c ? kStoreTma : (c_vec ? kStoreVec : kStoreScalar);
     const CUtensorMap& mc = map_c ? *map_c : map_a;   // unused unless cm == kStoreTma
-    const int sp = split.splits > 1 ? split.splits : 1;
-    const int kps = sp > 1 ? split.k_per_split : 0, wr = sp > 1 ? split.ws_rows : 0;
+    const CUtensorMap& mw = map_w ? *map_w : map_a;   // unused without split units
+    const int kps = splitting ? split.k_per_split : 0, wt = (int)whole;
     cudaError_t e;
     if (mode == TcMode::kBF16 && !b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, mw,
+                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
     else if (mode == TcMode::kTF32 && b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, mw,
+                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
     else if (mode == TcMode::kF16 && !b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, C,
-                               M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wr, err, limit_ns);
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, mw,
+                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
     else
         return cudaErrorInvalidValue;
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+int64_t tc_split_workspace_bytes(const TcSplit& split, int64_t M, int64_t N) {
+    if (split.splits < 2) return 0;
+    const int64_t pairs = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+    return (pairs - split.whole_tiles) * split.splits * (int64_t)(2 * kBM) * (2 * kBM) * 4;
+}
+
+cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* C, int M, int N,
+                                  bool c_vec, const Epilogue& epi, cudaStream_t stream) {
+    const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
+    const int64_t pairs = (int64_t)pairs_m * tiles_n;
+    const int64_t split_tiles = pairs - split.whole_tiles;
+    if (split.splits < 2 || split_tiles <= 0 || split.whole_tiles < 0) return cudaErrorInvalidValue;
+    const int64_t units = split_tiles * (2 * kBM) * (2 * kBM / 4);
+    const int64_t blocks = (units + 255) / 256;
+    const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
+    tile_reduce_kernel<<<grid, 256, 0, stream>>>(ws, split.splits, split.whole_tiles,
+                                                 (int)split_tiles, pairs_m, tiles_n, C, M, N,
+                                                 c_vec ? 1 : 0, epi);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
