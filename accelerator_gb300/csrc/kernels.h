@@ -8,6 +8,11 @@
 
 namespace libgemm {
 
+// Launch the tensor-core kernel and the split fix-ups with programmatic
+// stream serialization, so that their set-up overlaps the end of the kernel
+// before them (each waits for that kernel before touching global memory).
+constexpr bool kUsePdl = true;
+
 // What every kernel does with a finished sum acc of C_ij:
 //   kind 0  C_ij := acc                          (C is not read)
 //   kind 1  C_ij := alpha * acc, rounded once    (C is not read)

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
                                                            float* __restrict__ dst, int64_t rows,
                                                            int64_t cols, int64_t dst_ld) {
     __shared__ float tile[64][65];
+    grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
     const int t = threadIdx.x;
     const int64_t c0 = (int64_t)blockIdx.x * 64;   // src column = dst row
     const int64_t cols4 = cols / 4;
@@ -120,6 +121,7 @@ struct Bf16Job {
 };
 
 __global__ void __launch_bounds__(256) to_bf16_pair_kernel(Bf16Job a, Bf16Job b) {
+    grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
     const int64_t total = a.rows + b.rows;
     for (int64_t rr = blockIdx.x; rr < total; rr += gridDim.x) {
         const bool in_a = rr < a.rows;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(256)
     constexpr int W = kVec ? 4 : 1;
     const int64_t nw = (N + W - 1) / W, units = M * nw;
     const int64_t sstride = ws_rows * ws_ld;
+    grid_dependency_wait();   // the partials' kernel is complete and its writes visible
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = u / nw, j = (u - i * nw) * W;
@@ -355,11 +358,21 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, i
     const int64_t units = M * (vec ? N / 4 : N);
     const int64_t blocks = (units + 255) / 256;
     const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
-    if (vec)
-        splitk_reduce_kernel<true><<<grid, 256, 0, stream>>>(ws, splits, ws_rows, ws_ld, C, M, N, epi);
-    else
-        splitk_reduce_kernel<false><<<grid, 256, 0, stream>>>(ws, splits, ws_rows, ws_ld, C, M, N, epi);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = kUsePdl ? 1 : 0;
+    const cudaError_t e =
+        vec ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, ws, splits, ws_rows, ws_ld, C, M,
+                                 N, epi)
+            : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, ws, splits, ws_rows, ws_ld, C,
+                                 M, N, epi);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream) {

@@ -240,6 +240,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 // All threads of all CTAs of the cluster.
+// Programmatic dependent launch.  grid_dependency_wait blocks until the
+// grid this one was launched after (with programmatic stream
+// serialization) has completed and its memory operations are visible; it
+// returns at once when there is no such grid.  grid_launch_dependents lets
+// the next grid on the stream be scheduled before this one exits.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -419,6 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();   // both CTAs' barriers and TMEM exist before anyone signals the other
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above touched only this cluster's shared memory and TMEM, so
+    // it may overlap the end of the previous kernel on the stream; from here
+    // on global memory (A, B, C, the workspace) is read and written.
+    grid_dependency_wait();
 
     const int npairs = pairs_m * tiles_n;
     const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
@@ -484,6 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
             }
+            // every load of this CTA is issued: the next kernel (the split
+            // fix-up) may be scheduled now; it waits for this grid to finish
+            grid_launch_dependents();
             // Each copy issued here must have landed before the CTA exits: a
             // slot's copy has been consumed once the MMAs that read it freed it.
             for (int s = 0; s < kPStages; ++s)
@@ -632,6 +639,7 @@ __global__ void __launch_bounds__(256)
     constexpr int64_t kPerTile = (int64_t)kTile * (kTile / 4);
     constexpr int64_t kBlock = (int64_t)kTile * kTile;
     const int64_t units = (int64_t)split_tiles * kPerTile;
+    grid_dependency_wait();   // the MMA kernel's partials are complete and visible
     for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
          u += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(u / kPerTile);
@@ -807,13 +815,15 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kPSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kUsePdl ? 2 : 1;
     const int cm = map_c ? kStoreTma : (c_vec ? kStoreVec : kStoreScalar);
     const CUtensorMap& mc = map_c ? *map_c : map_a;   // unused unless cm == kStoreTma
     const CUtensorMap& mw = map_w ? *map_w : map_a;   // unused without split units
@@ -848,10 +858,19 @@ cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* 
     const int64_t units = split_tiles * (2 * kBM) * (2 * kBM / 4);
     const int64_t blocks = (units + 255) / 256;
     const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
-    tile_reduce_kernel<<<grid, 256, 0, stream>>>(ws, split.splits, split.whole_tiles,
-                                                 (int)split_tiles, pairs_m, tiles_n, C, M, N,
-                                                 c_vec ? 1 : 0, epi);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = kUsePdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, tile_reduce_kernel, ws, split.splits,
+                                             split.whole_tiles, (int)split_tiles, pairs_m, tiles_n,
+                                             C, M, N, c_vec ? 1 : 0, epi);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
