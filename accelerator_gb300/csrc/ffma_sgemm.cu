@@ -391,19 +391,21 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
     p.dp_tiles = tiles;
     p.splits = 1;
     const int64_t rem = slots > 0 ? tiles % slots : 0;
-    // Few tiles and a long K: more pieces than the in-kernel combination
-    // handles well.  Every tile is split (at least kMinSlabs slabs a piece,
-    // one wave, at most 256 pieces and kMaxWorkspace bytes of partials), each
-    // piece stores its partial as a whole M x N block, and a second kernel
-    // adds the blocks in piece order.
+    // Fewer tiles than one wave holds: every tile is split (at least
+    // kMinSlabsWide slabs a piece, one wave, at most 256 pieces and
+    // kMaxWorkspace bytes of partials), each piece stores its partial as a
+    // whole M x N block, and a second kernel adds the blocks in piece order.
+    // (Its loads are independent of one another; the in-kernel combination,
+    // kept for the split tiles of a last wave, is latency-bound: 2 splits of
+    // a 256^3 product took 53 us in the kernel against 24 us this way.)
     constexpr int64_t kMinSlabsWide = 4, kMaxWorkspace = 512ll << 20;
-    if (slots > 0 && tiles < slots && slots / tiles > 16 && nkt / kMinSlabsWide > 16) {
+    if (slots > 0 && tiles < slots && slots / tiles >= 2 && nkt >= 2 * kMinSlabsWide) {
         int64_t s = slots / tiles;
         if (s > nkt / kMinSlabsWide) s = nkt / kMinSlabsWide;
         if (s > 256) s = 256;
         const int64_t block = (int64_t)M * N * (int64_t)sizeof(float);
         if (s * block > kMaxWorkspace) s = kMaxWorkspace / block;
-        if (s > 16) {
+        if (s >= 2) {
             p.splits = (int)s;
             p.dp_tiles = 0;
             p.split_tiles = tiles;
@@ -412,10 +414,11 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
             return p;
         }
     }
-    // Split the tiles of a partial last wave along K, as many ways as still
-    // fit in one wave, keeping at least kMinSlabs slabs per piece.
+    // Split the tiles of a partial last wave (after at least one full wave)
+    // along K, as many ways as still fit in one wave, keeping at least
+    // kMinSlabs slabs per piece; the last piece of a tile adds them up.
     constexpr int64_t kMinSlabs = 8;
-    if (rem > 0) {
+    if (rem > 0 && tiles > slots) {
         int64_t s = slots / rem;
         if (s > nkt / kMinSlabs) s = nkt / kMinSlabs;
         if (s > 16) s = 16;

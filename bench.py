@@ -483,6 +483,58 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
             "overlap": "copy-in, compute and copy-out on three streams"}
 
 
+def run_sweep(args):
+    """The square sweep: N = 128 .. 4096 in every mode (and 8192 on the tensor
+    modes), U[0,1) inputs, L2 flushed before each launch, `warmup` untimed
+    launches then the median of `steps` CUDA-event-timed launches per (N,
+    mode).  Prints one JSON line holding the table; not a bench line."""
+    import torch
+    from accelerator_gb300 import binding, build, inputs
+    torch.cuda.set_device(0)
+    build.build()
+    dev = torch.device("cuda", 0)
+    _, bf16_peak, _, src = _measured_peaks()
+    peaks = {"fp32": (fp32_ffma_peak(), "alu"), "tf32": (bf16_peak * TF32_PER_BF16, "tensor"),
+             "bf16": (bf16_peak, "tensor")}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for n in (128, 256, 512, 1024, 2048, 4096, 8192):
+        A, B = inputs.matrices(n, n, n, "u01")
+        a32, b32 = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+        a16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16).to(dev)
+        b16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16).to(dev)
+        C = torch.zeros((n, n), dtype=torch.float32, device=dev)
+        for m in args.modes:
+            if n > 4096 and m == "fp32":
+                continue
+            a, b = (a16, b16) if m == "bf16" else (a32, b32)
+            mode = binding.MODES[m]
+            times = []
+            for r in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                binding.gemm(a, b, C, mode=mode, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if r >= args.warmup:
+                    times.append(e0.elapsed_time(e1))
+            if binding.debug_status(stream) != binding.OK:
+                raise RuntimeError(f"a kernel reported a timeout at N={n} {m}")
+            ms = float(np.median(times))
+            tf = flops(n, n, n) / (ms / 1e3) / 1e12
+            peak, bound = peaks[m]
+            rows.append({"n": n, "mode": m, "ms_median": ms, "tflops": tf, "bound": bound,
+                         "peak": peak, "frac": tf / peak})
+        del a32, b32, a16, b16, C
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": rows, "unit": UNIT, "peak_source": src, "warmup": args.warmup,
+                      "repeats": args.steps, "l2": "flushed before every launch",
+                      "data": "synthetic U[0,1), seed 42"}), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -492,6 +544,8 @@ def main(argv=None):
     p.add_argument("--size", type=int, default=4096)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="print the square sweep N = 128 .. 8192 instead of the bench line")
     p.add_argument("--modes", default=",".join(MODES),
                    help="comma-separated subset of fp32,tf32,bf16 (default: all three; "
                         "a subset is for profiling single kernels, not a bench line)")
@@ -503,6 +557,8 @@ def main(argv=None):
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_libgemm(args)
 
 

@@ -42,7 +42,10 @@ struct CUstream_st; /* the type behind cudaStream_t */
 enum gemm_mode {
     /* A, B: const float*.  Exact binary32 arithmetic on the CUDA cores: every
      * product-accumulate is one fused multiply-add rounded to nearest, k
-     * ascending for each C_ij. */
+     * ascending for each C_ij.  When the output tiles do not fill the GPU
+     * and K is long, the library cuts K into consecutive ranges, runs the
+     * chain over each range and adds the range sums in range order (binary32
+     * adds): the same result on every run of the same shape. */
     GEMM_FP32 = 0,
     /* A, B: const float*.  Tensor cores (tcgen05, kind::tf32): the inputs are
      * read as TF32 (sign, 8-bit exponent, top 10 fraction bits of each

@@ -96,12 +96,13 @@ def test_large_8192_sampled(libgemm, mode):
     _sampled_case(libgemm, 8192, 8192, 8192, "pm1", mode)
 
 
-@pytest.mark.parametrize("M,K,N", [(1000, 240, 1500), (257, 129, 383), (128, 16, 128),
-                                   (4096, 64, 4096), (3, 1, 5)])
+@pytest.mark.parametrize("M,K,N", [(1000, 112, 1500), (257, 100, 383), (128, 16, 128),
+                                   (4096, 64, 4096), (3, 1, 5), (2048, 240, 2048)])
 def test_fp32_is_the_binary32_fma_chain(libgemm, M, K, N):
     """FP32 mode, bit for bit: each C_ij is acc = fma(A_ik, B_kj, acc), k
-    ascending.  (K <= 240 is 15 slabs of 16, too few for the library to
-    split a tile's K range.)"""
+    ascending, wherever the library keeps a tile's K range whole: K < 128
+    (under 8 slabs of 16), or a tile count of half a wave or more that does
+    not exceed one wave (2048^2: 256 tiles of 128 x 128)."""
     A, B = inputs.matrices(M, K, N, "pm1", seed=M + 7 * K + 13 * N)
     C = run(libgemm, A, B, "fp32")
     np.testing.assert_array_equal(C, oracle.fma_chain(A, B))
