@@ -47,6 +47,19 @@ def test_ragged_1000x777x1500_pm1(libgemm, oracle_cache, mode):
     _full_case(libgemm, oracle_cache, 1000, 777, 1500, "pm1", mode)
 
 
+@pytest.mark.parametrize("mode", MODES + ["fp32_via_bf16"])
+def test_pages_non_square_exercise(libgemm, oracle_cache, mode):
+    # "Matrix Multiplication -- Naive to Tiled", section 08, exercise 1: A of
+    # 512 x 768 times B of 768 x 1024, entries uniform on [0, 1)
+    if mode == "fp32_via_bf16":
+        A, B = inputs.matrices(512, 768, 1024, "u01")
+        C = run(libgemm, A, B, mode)
+        Cref, S = oracle_cache.full((512, 768, 1024, "u01"), A, B)
+        assert_within(C, Cref, S, TOL[mode], "fp32_via_bf16 512x768x1024")
+    else:
+        _full_case(libgemm, oracle_cache, 512, 768, 1024, "u01", mode)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_ragged_integers_bit_exact(libgemm, oracle_cache, mode):
     # |C| <= 777 * 16 < 2**24 and every partial sum is an integer: exact in binary32
