@@ -53,6 +53,16 @@ def matrix_c(M: int, N: int, dist: str = "pm1", seed: int = BASE_SEED):
     return _draw(rc, (M, N), dist)
 
 
+def int_pattern(row0: int, rows: int, cols: int, a: int = 7, b: int = 3) -> np.ndarray:
+    """Rows row0 .. row0 + rows - 1 of a deterministic integer matrix with
+    entries ((a * i + b * k + 1) mod 9) - 4 in [-4, 4], as float32: cheap to
+    make block by block for operands too large to draw at once, and exact in
+    binary32, TF32, bfloat16 and binary16."""
+    i = (np.arange(row0, row0 + rows, dtype=np.int64) * a) % 9
+    k = (np.arange(cols, dtype=np.int64) * b + 1) % 9
+    return (((i[:, None] + k[None, :]) % 9) - 4).astype(np.float32)
+
+
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (to nearest, ties to even); uint16 patterns.
 
