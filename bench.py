@@ -204,6 +204,24 @@ def _dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device="cpu") -> float:
+    """The largest x over all ranks (x itself with one rank).  The timed
+    figure of a multi-rank run is the slowest rank's."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(ws: int, products_per_rank: int, flops_per_product: float, ms: float) -> float:
+    """Whole-job throughput: the products all ranks completed over the
+    slowest rank's time (replicas: every rank does the same work)."""
+    return ws * products_per_rank * flops_per_product / (ms / 1e3) / 1e12
+
+
 def _cpu_sample(A: np.ndarray, B: np.ndarray, fmt: str, rows: int):
     """fp64 oracle on the first `rows` rows of C; returns seconds."""
     import oracle
@@ -331,12 +349,8 @@ def run_libgemm(args):
     launches = binding.launch_count() - launches0
     per_mode = {m: np.array([evs[s][m][0].elapsed_time(evs[s][m][1]) for s in range(args.steps)])
                 for m in args.modes}
-    ms_step = float(np.mean(sum(per_mode[m] for m in args.modes)))
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = ws * len(args.modes) * f / (ms_step / 1e3) / 1e12
+    ms_step = max_over_ranks(float(np.mean(sum(per_mode[m] for m in args.modes))), ws, dev)
+    value = job_tflops(ws, len(args.modes), f, ms_step)
     if binding.debug_status(stream) != binding.OK:
         raise RuntimeError("a kernel reported a timeout during the timed region")
     clk = clocks.summary()
