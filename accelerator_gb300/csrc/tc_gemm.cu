@@ -336,6 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 //           and to both CTAs' accumulator-full barriers after a tile.
 //   warps 2-5  epilogue of this CTA's rows; each warp then arrives on the
 //           leader's accumulator-empty barrier (count 8: 4 warps x 2 CTAs).
+// Work units: pair tiles, or (tile, K range) pieces of the tiles a K split
+// cuts up, whose raw partial sums go to a workspace for tile_reduce_kernel.
+// Launched with programmatic stream serialisation: the set-up above the
+// grid dependency wait overlaps the previous kernel; no global memory is
+// touched before it.
 constexpr int kPStages = 6;
 
 // Pair tile p of the pair kernel's grouped raster: rows m0 .. m0 + 255,
