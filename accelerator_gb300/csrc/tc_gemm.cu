@@ -35,6 +35,9 @@
 // Every wait is bounded (see mbar_wait): if one expires the CTA records a
 // timeout in the device error word, the roles stop, in-flight copies and
 // MMAs are drained with bounded waits, TMEM is freed and the CTA returns.
+#include <cstdlib>
+#include <cstring>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -740,6 +743,10 @@ cudaError_t tc_setup() {
     const int a = query_max_pairs<TcMode::kBF16, false>(sms);
     const int b = query_max_pairs<TcMode::kTF32, true>(sms);
     g_max_pairs = a < b ? a : b;
+    // GEMM_FORCE_CONFIG=single_cta: use the 1-SM kernel even where pairs fit
+    // (it is otherwise only taken on devices that cannot hold pair clusters).
+    const char* force = std::getenv("GEMM_FORCE_CONFIG");
+    if (force && std::strcmp(force, "single_cta") == 0) g_max_pairs = 0;
     return cudaSuccess;
 }
 
