@@ -51,6 +51,7 @@ FP32_LANES_PER_SM = 128                      # FFMA lanes per SM (4 sub-partitio
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 TF32_PER_BF16 = 1.1 / 2.25                   # nominal dense TF32 / BF16 tensor rates
+NOMINAL_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0}   # stated dense peaks (no sparsity)
 
 # DRAM traffic of one launch of the dominant kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
@@ -384,6 +385,7 @@ def run_libgemm(args):
         modes_out[m] = {"ms_mean": ms, "ms_median": float(np.median(per_mode[m])),
                         "tflops": achieved, "bound": bound, "peak": peak, "frac": achieved / peak,
                         "peak_source": note}
+        modes_out[m]["frac_nominal"] = achieved / NOMINAL_TFLOPS.get(m, fp32_ffma_peak())
         if m == "fp32" and sm_mhz:
             modes_out[m]["frac_at_observed_clock"] = achieved / fp32_ffma_peak(sm_mhz)
     dom = max(args.modes, key=lambda m: modes_out[m]["ms_mean"])
@@ -497,6 +499,39 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
             "overlap": "copy-in, compute and copy-out on three streams"}
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_cpu_sweep(args):
+    """The fp64 oracle on the host cores, full C: one core for N <= 2048 and
+    all cores for N <= 4096, on the sweep's inputs (U[0,1), seed 42).  Prints
+    one JSON line; not a bench line."""
+    import oracle
+    from accelerator_gb300 import inputs
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rows = []
+    for n in (128, 256, 512, 1024, 2048, 4096):
+        A, B = inputs.matrices(n, n, n, "u01")
+        for threads in ((1, cores) if n <= 2048 else (cores,)):
+            used = oracle.threads(threads)
+            t0 = time.perf_counter()
+            oracle.gemm(A, B, "f32", nthreads=threads)
+            dt = time.perf_counter() - t0
+            rows.append({"n": n, "threads": used, "seconds": dt, "gflops": flops(n, n, n) / dt / 1e9})
+    print(json.dumps({"cpu_sweep": rows, "kind": "oracle", "cpu_model": _cpu_model(),
+                      "cores_available": cores, "data": "synthetic U[0,1), seed 42"}), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """The square sweep: N = 128 .. 4096 in every mode (and 8192 on the tensor
     modes), U[0,1) inputs, L2 flushed before each launch, `warmup` untimed
@@ -560,6 +595,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sweep", action="store_true",
                    help="print the square sweep N = 128 .. 8192 instead of the bench line")
+    p.add_argument("--cpu-sweep", action="store_true",
+                   help="print the fp64 oracle's timings on the host cores, N = 128 .. 4096")
     p.add_argument("--modes", default=",".join(MODES),
                    help="comma-separated subset of fp32,tf32,bf16 (default: all three; "
                         "a subset is for profiling single kernels, not a bench line)")
@@ -571,6 +608,8 @@ def main(argv=None):
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.cpu_sweep:
+        return run_cpu_sweep(args)
     if args.sweep:
         return run_sweep(args)
     return run_libgemm(args)
