@@ -149,7 +149,8 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
     else
         g_launches++;
     if (rc == GEMM_OK && plan.wide) {
-        if (launch_splitk_reduce(ws, plan.splits, M, N, C, M, N, c_vec, epi, stream) != cudaSuccess)
+        if (launch_splitk_reduce(ws, plan.splits, M, N, C, M, N, c_vec, epi, st->num_sms, stream) !=
+            cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
             g_launches++;
@@ -191,7 +192,7 @@ int split_tc_launch(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
     }
     if (rc == GEMM_OK) {
         if (launch_tc_tile_reduce(static_cast<const float*>(ws), split, C, (int)M, (int)N, c_vec,
-                                  epi, stream) != cudaSuccess)
+                                  epi, st->num_sms, stream) != cudaSuccess)
             rc = GEMM_ERR_CUDA;
         else
             g_launches++;

@@ -109,12 +109,12 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
 // C := the epilogue applied to the sum, in split order, of the workspace
 // blocks of every split tile (the whole tiles are left as they are).
 cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* C, int M, int N,
-                                  bool c_vec, const Epilogue& epi, cudaStream_t stream);
+                                  bool c_vec, const Epilogue& epi, int num_sms, cudaStream_t stream);
 // C (M x N) := the epilogue applied to the sum, in split order, of the
 // partials ws[s * ws_rows + i][j] (row stride ws_ld floats).
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
                                  float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
-                                 cudaStream_t stream);
+                                 int num_sms, cudaStream_t stream);
 // b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
 cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,

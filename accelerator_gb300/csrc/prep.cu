@@ -350,14 +350,15 @@ cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream) {
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
                                  float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
-                                 cudaStream_t stream) {
+                                 int num_sms, cudaStream_t stream) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (splits < 1 || ws_rows < M || ws_ld < N) return cudaErrorInvalidValue;
     const bool vec = c_vec && N % 4 == 0 && ws_ld % 4 == 0 &&
                      (reinterpret_cast<uintptr_t>(ws) & 15u) == 0;
     const int64_t units = M * (vec ? N / 4 : N);
     const int64_t blocks = (units + 255) / 256;
-    const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
+    const int64_t cap = (int64_t)num_sms * 16;   // two rounds of 8 resident 256-thread blocks
+    const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(256);

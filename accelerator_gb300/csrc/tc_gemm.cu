@@ -862,14 +862,16 @@ int64_t tc_split_workspace_bytes(const TcSplit& split, int64_t M, int64_t N) {
 }
 
 cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* C, int M, int N,
-                                  bool c_vec, const Epilogue& epi, cudaStream_t stream) {
+                                  bool c_vec, const Epilogue& epi, int num_sms,
+                                  cudaStream_t stream) {
     const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
     const int64_t pairs = (int64_t)pairs_m * tiles_n;
     const int64_t split_tiles = pairs - split.whole_tiles;
     if (split.splits < 2 || split_tiles <= 0 || split.whole_tiles < 0) return cudaErrorInvalidValue;
     const int64_t units = split_tiles * (2 * kBM) * (2 * kBM / 4);
     const int64_t blocks = (units + 255) / 256;
-    const unsigned grid = (unsigned)(blocks < 152 * 16 ? blocks : 152 * 16);
+    const int64_t cap = (int64_t)num_sms * 16;   // two rounds of 8 resident 256-thread blocks
+    const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(256);
