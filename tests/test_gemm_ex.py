@@ -112,9 +112,12 @@ def test_k_zero_is_beta_c(libgemm, alpha, beta):
 
 @pytest.mark.parametrize("mode", ["fp32", "bf16", "tf32"])
 def test_split_and_large_shapes(libgemm, mode):
-    """A shape whose FP32 last wave is split in K (partials summed, then the
-    update), and a 2048^3 product checked on sampled entries."""
-    for (M, K, N) in [(640, 2048, 640), (2048, 2048, 2048)]:
+    """Shapes whose tiles are all split in K (640 x 2048 x 640), none
+    (2048^3), and only the last wave's or round's (4096^3: the whole tiles
+    apply the update in the GEMM kernel, the split ones after the partials
+    are added), checked on sampled entries, corners and last row and column
+    included."""
+    for (M, K, N) in [(640, 2048, 640), (2048, 2048, 2048), (4096, 4096, 4096)]:
         A, B = inputs.matrices(M, K, N, "pm1", seed=K + 1)
         C_in = inputs.matrix_c(M, N, "pm1", seed=K + 1)
         out = run_ex(libgemm, A, B, C_in, 0.5, -2.0, mode)
