@@ -51,6 +51,8 @@ class GemmError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded libgemm.so.  Raises if it has not been built."""
     global _lib
+    if _lib is not None:          # loaded: no lock needed to read it
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.LIB
@@ -123,12 +125,18 @@ def gemm_ex(A, B, C=None, alpha=1.0, beta=0.0, mode=FP32, stream=None):
     return C
 
 
+_WANT = {}   # mode -> the operand dtype, filled at the first call
+
+
 def _operands(A, B, C, mode):
     """Checks the tensors of a call; returns (mode number, C or a new C)."""
     import torch
     if isinstance(mode, str):
         mode = MODES[mode.lower()]
-    want = {BF16: torch.bfloat16, FP16: torch.float16}.get(mode, torch.float32)
+    if not _WANT:
+        _WANT.update({FP32: torch.float32, TF32: torch.float32, BF16: torch.bfloat16,
+                      FP16: torch.float16, FP32_VIA_BF16: torch.float32})
+    want = _WANT.get(mode, torch.float32)
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shapes {tuple(A.shape)} and {tuple(B.shape)} do not chain")
     for name, t in (("A", A), ("B", B)):
