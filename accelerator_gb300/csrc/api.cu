@@ -277,7 +277,7 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
             a_use = s;
         }
         if (rc == GEMM_OK && b_bytes > 0) {
-            cudaError_t e = b_k_major ? launch_transpose(B, s + a_bytes, K, N, ldb, es, stream)
+            cudaError_t e = b_k_major ? launch_transpose(B, s + a_bytes, K, N, ldb, es, st->num_sms, stream)
                                       : launch_restride(B, s + a_bytes, K, N, N, ldb, es, stream);
             if (e != cudaSuccess) rc = GEMM_ERR_CUDA;
             g_launches++;

@@ -128,7 +128,7 @@ cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t co
                             int64_t src_ld, int64_t dst_ld, int es, cudaStream_t stream);
 // dst (cols x rows, row stride dst_ld elements) = transpose of src (rows x cols, dense).
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
-                             int64_t dst_ld, int es, cudaStream_t stream);
+                             int64_t dst_ld, int es, int num_sms, cudaStream_t stream);
 // dst (rows x cols bfloat16, row stride dst_ld elements) = round-to-nearest-
 // even of src (rows x cols float, dense).
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,

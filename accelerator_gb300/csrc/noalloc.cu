@@ -115,7 +115,7 @@ extern "C" int gemm_tf32_noalloc(const float* A, const float* B, float* C, int64
         a_use = s;
     }
     void* bt = s + a_bytes;
-    if (launch_transpose(B, bt, K, N, ld, 4, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_transpose(B, bt, K, N, ld, 4, num_sms, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     count_launch();
 
     const TcShape shape = tc_shape(TcMode::kTF32);

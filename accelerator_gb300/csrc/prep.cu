@@ -56,7 +56,10 @@ __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst,
 
 // Vector form for 32-bit elements when B's rows are 16-byte aligned
 // (cols % 4 == 0, 16-byte aligned base) and dst_ld % 4 == 0: 64 x 64 tiles,
-// every global access 16 bytes wide, 4 loads in flight per thread.  Rows
+// every global access 16 bytes wide.  Persistent blocks walk the tiles; the
+// loads of a block's next tile are issued before it writes out the current
+// one, so they are in flight during the writes (one tile per block left
+// each block's loads exposed, and a partial last wave).  Rows
 // beyond `rows` read as zero; dst columns up to roundup(rows, 4) are written
 // (the padding is inside dst's row stride and is never read as data).
 __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restrict__ src,
@@ -65,15 +68,20 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
     __shared__ float tile[64][65];
     grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
     const int t = threadIdx.x;
-    const int64_t c0 = (int64_t)blockIdx.x * 64;   // src column = dst row
-    const int64_t cols4 = cols / 4;
-    for (int64_t r0 = (int64_t)blockIdx.y * 64; r0 < rows; r0 += (int64_t)gridDim.y * 64) {
-        float4 v[4];
+    const int64_t tiles_c = (cols + 63) / 64, tiles_r = (rows + 63) / 64;
+    const int64_t ntiles = tiles_c * tiles_r, cols4 = cols / 4;
+    float4 v[4];
+    auto load = [&](int64_t tl, float4 (&w)[4]) {
+        const int64_t c0 = (tl % tiles_c) * 64, r0 = (tl / tiles_c) * 64;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {               // src rows r0 + t/16 + 16p, columns c0 + 4(t%16)
+        for (int p = 0; p < 4; ++p) {
             const int64_t r = r0 + t / 16 + 16 * p, c4 = c0 / 4 + t % 16;
-            v[p] = (r < rows && c4 < cols4) ? src[r * cols4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            w[p] = (r < rows && c4 < cols4) ? src[r * cols4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    int64_t tl = blockIdx.x;
+    if (tl < ntiles) load(tl, v);
+    for (; tl < ntiles; tl += gridDim.x) {
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int rr = t / 16 + 16 * p, cc = 4 * (t % 16);
@@ -81,11 +89,14 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
             tile[rr][cc + 2] = v[p].z, tile[rr][cc + 3] = v[p].w;
         }
         __syncthreads();
+        const int64_t next = tl + gridDim.x;
+        if (next < ntiles) load(next, v);   // in flight while this tile is written out
+        const int64_t c0 = (tl % tiles_c) * 64, r0 = (tl / tiles_c) * 64;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {               // dst row c0 + t/16 + 16p, columns r0 + 4(t%16)
+        for (int p = 0; p < 4; ++p) {
             const int dr = t / 16 + 16 * p, dk = 4 * (t % 16);
             const int64_t row = c0 + dr, k = r0 + dk;
-            if (row < cols && k < rows)             // k < rows: the chunk starts inside src
+            if (row < cols && k < rows)
                 *reinterpret_cast<float4*>(dst + row * dst_ld + k) =
                     make_float4(tile[dk][dr], tile[dk + 1][dr], tile[dk + 2][dr], tile[dk + 3][dr]);
         }
@@ -260,13 +271,13 @@ cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t co
 }
 
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
-                             int64_t dst_ld, int es, cudaStream_t stream) {
+                             int64_t dst_ld, int es, int num_sms, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
     if (es == 4 && cols % 4 == 0 && dst_ld % 4 == 0 &&
         (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-        const int64_t vx = (cols + 63) / 64, vy = (rows + 63) / 64;
-        if (vx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-        dim3 vgrid((unsigned)vx, (unsigned)(vy < 65535 ? vy : 65535));
+        const int64_t ntiles = ((cols + 63) / 64) * ((rows + 63) / 64);
+        const int64_t cap = (int64_t)num_sms * 8;   // persistent: 8 resident blocks per SM
+        const unsigned vgrid = (unsigned)(ntiles < cap ? ntiles : cap);
         transpose_v4_kernel<<<vgrid, 256, 0, stream>>>(static_cast<const float4*>(src),
                                                        static_cast<float*>(dst), rows, cols, dst_ld);
         return cudaGetLastError();
