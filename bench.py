@@ -57,8 +57,8 @@ NOMINAL_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0}   # stated dense peaks (no spa
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
 # kernel source it was taken on; reported as null once the source changes.
 TRAFFIC = {
-    # profiles/ffma_sgemm_fp32_4096.md: 336.2 MB read + 69.2 MB written
-    "ffma_sgemm.cu": ("ff673082ea694ae22555f3b924c99186edd474260ca913baaada41164a84321e", 405.4e6),
+    # profiles/ffma_sgemm_fp32_4096.md: 336.5 MB read + 69.4 MB written
+    "ffma_sgemm.cu": ("640345fe0fa0d6a8485ef2b8edf5d3200c008696635ef04a6cabf161d7c38d80", 405.9e6),
 }
 
 
@@ -81,9 +81,15 @@ def _measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
-def fp32_ffma_peak(mhz: float = SM_MAX_MHZ) -> float:
+def fp32_ffma_peak(mhz: float = SM_MAX_MHZ, sms: int = NUM_SMS) -> float:
     """FP32 FFMA peak in TFLOP/s: SMs x lanes x 2 FLOP x clock."""
-    return NUM_SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def device_sms(dev) -> int:
+    """The device's SM count (152 on GB300)."""
+    import torch
+    return int(torch.cuda.get_device_properties(dev).multi_processor_count)
 
 
 def _src_hash(name: str) -> str:
@@ -372,12 +378,15 @@ def run_libgemm(args):
     hbm, bf16_peak, bf16_sus, src = _measured_peaks()
     tf32_peak = bf16_peak * TF32_PER_BF16
     sm_mhz = clk["sm_mhz"] if clk else None
+    max_mhz = float(clk["sm_max_mhz"]) if clk and clk.get("sm_max_mhz") else SM_MAX_MHZ
+    sms = device_sms(dev)
     modes_out = {}
     for m in args.modes:
         ms = float(np.mean(per_mode[m]))
         achieved = f / (ms / 1e3) / 1e12
         if m == "fp32":
-            peak, bound, note = fp32_ffma_peak(), "alu", "FP32 FFMA: 152 SMs x 128 lanes x 2 x 2070 MHz"
+            peak, bound = fp32_ffma_peak(max_mhz, sms), "alu"
+            note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 x {max_mhz:.0f} MHz (device SM count, NVML max SM clock)"
         elif m == "tf32":
             peak, bound, note = tf32_peak, "tensor", f"{src} bf16 x nominal tf32/bf16 ratio"
         else:
@@ -385,9 +394,9 @@ def run_libgemm(args):
         modes_out[m] = {"ms_mean": ms, "ms_median": float(np.median(per_mode[m])),
                         "tflops": achieved, "bound": bound, "peak": peak, "frac": achieved / peak,
                         "peak_source": note}
-        modes_out[m]["frac_nominal"] = achieved / NOMINAL_TFLOPS.get(m, fp32_ffma_peak())
+        modes_out[m]["frac_nominal"] = achieved / NOMINAL_TFLOPS.get(m, fp32_ffma_peak(max_mhz, sms))
         if m == "fp32" and sm_mhz:
-            modes_out[m]["frac_at_observed_clock"] = achieved / fp32_ffma_peak(sm_mhz)
+            modes_out[m]["frac_at_observed_clock"] = achieved / fp32_ffma_peak(sm_mhz, sms)
     dom = max(args.modes, key=lambda m: modes_out[m]["ms_mean"])
     dom_file = "ffma_sgemm.cu" if dom == "fp32" else "tc_gemm.cu"
     traffic = None
@@ -543,7 +552,8 @@ def run_sweep(args):
     build.build()
     dev = torch.device("cuda", 0)
     _, bf16_peak, _, src = _measured_peaks()
-    peaks = {"fp32": (fp32_ffma_peak(), "alu"), "tf32": (bf16_peak * TF32_PER_BF16, "tensor"),
+    peaks = {"fp32": (fp32_ffma_peak(SM_MAX_MHZ, device_sms(dev)), "alu"),
+             "tf32": (bf16_peak * TF32_PER_BF16, "tensor"),
              "bf16": (bf16_peak, "tensor")}
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
