@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libgemm (include/gemm.h): argument checks, the
-// choice of kernel, TMA descriptors, scratch for re-strided operands, and the
-// device error word.  Host code only, apart from the error word itself.
+// per-device set-up, the choice of kernel and of a K split, TMA descriptors,
+// stream-ordered scratch (re-strided or rounded operands, split workspaces),
+// and the device error word.  Host code only, apart from the error word.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -20,6 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single pipeline wait
 
 struct DeviceState {
+    std::atomic<bool> done{false};   // set-up finished (read without the lock)
     bool ready = false;
     int status = GEMM_OK;
     int num_sms = 0;
@@ -57,8 +59,12 @@ int device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
-    std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& st = g_dev[dev];
+    if (st.done.load(std::memory_order_acquire)) {   // every later call: no lock
+        *out = &st;
+        return st.status;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
     if (!st.ready) {
         st.ready = true;
         int major = 0, minor = 0;
@@ -84,6 +90,7 @@ int device_state(DeviceState** out) {
                 g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         }
         if (st.status != GEMM_OK) cudaGetLastError();   // do not leave a stale error behind
+        st.done.store(true, std::memory_order_release);
     }
     *out = &st;
     return st.status;
