@@ -500,7 +500,7 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)   # the slowest rank's
     if binding.debug_status(stream) != binding.OK:
         raise RuntimeError("a kernel reported a timeout during the end-to-end run")
     return {"value": ws * len(args.modes) * f / (ms / 1e3) / 1e12, "unit": UNIT,
