@@ -58,10 +58,11 @@ def _offset_view(t, shape, offset_elems):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("which", ["A", "B", "C", "ABC"])
-def test_unaligned_bases(libgemm, mode, which):
-    """Bases aligned to the element size only (not to 16 bytes)."""
+@pytest.mark.parametrize("M,K,N", [(200, 136, 264), (256, 8192, 200)])
+def test_unaligned_bases(libgemm, mode, which, M, K, N):
+    """Bases aligned to the element size only (not to 16 bytes); the long-K
+    shape is split in K in every mode (workspaces and fix-up kernels)."""
     import torch
-    M, K, N = 200, 136, 264
     A, B = inputs.matrices(M, K, N, "pm1", seed=21)
     a, b = device_operands(A, B, mode)
     if "A" in which:
@@ -82,7 +83,7 @@ def test_no_writes_outside_c(libgemm, mode):
     """Canary bands on both sides of C stay untouched (a bounds check that
     needs no sanitizer)."""
     import torch
-    for (M, K, N) in [(1000, 777, 1500), (129, 65, 257), (1, 1, 1), (255, 33, 3)]:
+    for (M, K, N) in [(1000, 777, 1500), (129, 65, 257), (1, 1, 1), (255, 33, 3), (300, 9001, 203)]:
         A, B = inputs.matrices(M, K, N, "pm1", seed=3)
         a, b = device_operands(A, B, mode)
         guard = 4096
