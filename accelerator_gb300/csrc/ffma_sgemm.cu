@@ -4,8 +4,10 @@
 // opening formula), row-major as in "Matrix Multiplication -- Naive to
 // Tiled", section 02.  Every C_ij is one chain of fused multiply-adds with k
 // ascending, so the result is the sequential binary32 sum of exact products
-// (for the tiles of a partial last wave: the sum, in order, of such chains
-// over consecutive K ranges).
+// (when the tiles do not fill the GPU -- fewer than one wave, or a partial
+// last wave -- the sum, in order, of such chains over consecutive K ranges:
+// added in the kernel by the last CTA of a split tile after a full wave, or
+// by splitk_reduce_kernel from whole M x N partial blocks otherwise).
 //
 // Design (GB300 rather than the pages' 16x16/32x32 tiles):
 //   * A CTA owns a 128 x 128 tile of C and each thread a TM x TN register
