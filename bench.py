@@ -41,7 +41,12 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (FP32 and TF32/BF16) at N=4096, % of sm_103a peak"
 UNIT = "TFLOP/s"
-MODES = ("fp32", "tf32", "bf16")
+MODES = ("fp32", "tf32", "bf16")               # the bench line's step
+# further modes that --modes can select, to time or profile their kernels:
+# binary16 inputs (the BF16 kernel's kind::f16 with f16 operands) and FP32
+# data rounded to bfloat16 by a conversion launch before the BF16 kernel
+EXTRA_MODES = ("fp16", "fp32_via_bf16")
+ALL_MODES = MODES + EXTRA_MODES
 L2_FLUSH_BYTES = 256 << 20
 
 # GB300 facts used for the roofline denominators.
@@ -51,7 +56,8 @@ FP32_LANES_PER_SM = 128                      # FFMA lanes per SM (4 sub-partitio
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 TF32_PER_BF16 = 1.1 / 2.25                   # nominal dense TF32 / BF16 tensor rates
-NOMINAL_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0}   # stated dense peaks (no sparsity)
+NOMINAL_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0, "fp16": 2250.0,
+                  "fp32_via_bf16": 2250.0}   # stated dense peaks (no sparsity)
 
 # DRAM traffic of one launch of the dominant kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
@@ -317,7 +323,11 @@ def run_libgemm(args):
     a16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16).to(dev)
     b16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16).to(dev)
     ops = {"fp32": (a32, b32, binding.FP32), "tf32": (a32, b32, binding.TF32),
-           "bf16": (a16, b16, binding.BF16)}
+           "bf16": (a16, b16, binding.BF16), "fp32_via_bf16": (a32, b32, binding.FP32_VIA_BF16)}
+    if "fp16" in args.modes:
+        ops["fp16"] = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).view(torch.float16).to(dev),
+                       torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).view(torch.float16).to(dev),
+                       binding.FP16)
     C = torch.zeros((n, n), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -389,7 +399,9 @@ def run_libgemm(args):
             note = f"FP32 FFMA: {sms} SMs x 128 lanes x 2 x {max_mhz:.0f} MHz (device SM count, NVML max SM clock)"
         elif m == "tf32":
             peak, bound, note = tf32_peak, "tensor", f"{src} bf16 x nominal tf32/bf16 ratio"
-        else:
+        elif m == "fp32_via_bf16":
+            peak, bound, note = bf16_peak, "tensor", f"{src} bf16 burst (conversion launch included in the time)"
+        else:   # bf16, fp16: one kind::f16 rate
             peak, bound, note = bf16_peak, "tensor", f"{src} bf16 burst"
         modes_out[m] = {"ms_mean": ms, "ms_median": float(np.median(per_mode[m])),
                         "tflops": achieved, "bound": bound, "peak": peak, "frac": achieved / peak,
@@ -415,9 +427,9 @@ def run_libgemm(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp32+tf32+bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "+".join(args.modes), "data": "synthetic",
         "config": {"workload": f"square GEMM M=K=N={n}, one product per mode "
-                               "(fp32 FFMA, tf32 and bf16-input tcgen05), U[0,1) seed 42",
+                               f"({', '.join(args.modes)}), U[0,1) seed 42",
                    "l2": "flushed before every GEMM (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{ws}"},
         "modes": modes_out,
@@ -447,7 +459,10 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     hA16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).pin_memory()
     hB16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).pin_memory()
     modes = {"fp32": (hA, hB, binding.FP32), "tf32": (hA, hB, binding.TF32),
-             "bf16": (hA16, hB16, binding.BF16)}
+             "bf16": (hA16, hB16, binding.BF16), "fp32_via_bf16": (hA, hB, binding.FP32_VIA_BF16)}
+    if "fp16" in args.modes:
+        modes["fp16"] = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).pin_memory(),
+                         torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).pin_memory(), binding.FP16)
     # two sets of device buffers, used by alternate steps, so that a step's
     # copies need not wait for the previous step's product on the same mode
     bufs = [{}, {}]
@@ -481,6 +496,8 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
             xa, xb = b["xa"], b["xb"]
             if b["mode"] == binding.BF16:
                 xa, xb = xa.view(torch.bfloat16), xb.view(torch.bfloat16)
+            elif b["mode"] == binding.FP16:
+                xa, xb = xa.view(torch.float16), xb.view(torch.float16)
             binding.gemm(xa, xb, b["c"], mode=b["mode"], stream=stream)
             b["done"].record(stream)
             with torch.cuda.stream(s_out):
@@ -608,12 +625,16 @@ def main(argv=None):
     p.add_argument("--cpu-sweep", action="store_true",
                    help="print the fp64 oracle's timings on the host cores, N = 128 .. 4096")
     p.add_argument("--modes", default=",".join(MODES),
-                   help="comma-separated subset of fp32,tf32,bf16 (default: all three; "
-                        "a subset is for profiling single kernels, not a bench line)")
+                   help="comma-separated subset of " + ",".join(ALL_MODES) + " (default: "
+                        + ",".join(MODES) + ", the bench line; other selections time or "
+                        "profile single kernels)")
     args = p.parse_args(argv)
-    args.modes = tuple(m for m in MODES if m in args.modes.split(","))
+    unknown = [m for m in args.modes.split(",") if m not in ALL_MODES]
+    if unknown:
+        p.error(f"unknown mode(s) {unknown}; choose from {','.join(ALL_MODES)}")
+    args.modes = tuple(m for m in ALL_MODES if m in args.modes.split(","))
     if not args.modes:
-        p.error("--modes selects none of fp32, tf32, bf16")
+        p.error("--modes selects no mode")
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
