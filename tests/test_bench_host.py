@@ -30,3 +30,13 @@ def test_fp32_peak_arithmetic():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_mode_selection():
+    # unknown modes are refused before any GPU work; the extra modes exist
+    with pytest.raises(SystemExit):
+        bench.main(["--modes", "fp32,fp8"])
+    assert set(bench.EXTRA_MODES) <= set(bench.ALL_MODES)
+    assert bench.ALL_MODES[:3] == bench.MODES == ("fp32", "tf32", "bf16")
+    # every selectable mode has a stated nominal peak or the FFMA peak formula
+    assert all(m in bench.NOMINAL_TFLOPS for m in bench.ALL_MODES if m != "fp32")
