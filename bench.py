@@ -15,9 +15,10 @@ stream it runs on, so the flush is outside the measured time.  ms_per_step is
 the mean over steps of the three GEMMs' event times.  The JSON line also
 carries the roofline of the dominant kernel, the fp64 oracle's throughput on
 the host cores (cpu_baseline), an end-to-end figure with host buffers (every
-step copies each product's operands in from pinned host memory and its C back
-out; copy-in, compute and copy-out run on three streams so that one product's
-copies overlap another's compute), the SM clocks seen during the timed region
+step copies its inputs in from pinned host memory -- A and B as float32,
+shared by the FP32 and TF32 products, and as bfloat16 -- and every product's C
+back out; copy-in, compute and copy-out run on three streams so that one
+product's copies overlap another's compute), the SM clocks seen during the timed region
 and the number of library launches.
 
 ``--impl reference`` times the fp64 CPU oracle instead (a bounded sample of
@@ -373,9 +374,10 @@ def run_libgemm(args):
     clk = clocks.summary()
 
     # e2e: host buffers, copies inside the timed region.  Every step copies
-    # each product's operands in from pinned host memory and its C back out;
-    # three streams overlap one product's copies with another's compute, as a
-    # user of the library would.
+    # its inputs in from pinned host memory (once each, shared by the products
+    # that read them) and every product's C back out; three streams overlap
+    # one product's copies with another's compute, as a user of the library
+    # would.
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, A, B, n, dev, stream, ws, f)
@@ -447,64 +449,77 @@ def run_libgemm(args):
 
 
 def run_e2e(args, A, B, n, dev, stream, ws, f):
-    """E2E throughput: per step, for each mode, H2D of A and B (pinned host
-    memory), the product, and D2H of C, all inside the timed region.  The
-    copy-in stream, the compute stream and the copy-out stream are ordered by
-    events per mode and per buffer, so a buffer is only overwritten after its
-    previous use has finished."""
+    """E2E throughput: per step, the H2D copies of the step's inputs from
+    pinned host memory, one product per mode, and the D2H copy of every
+    product's C, all inside the timed region.  The inputs are copied once per
+    step and shared by the products that take them (A and B as float32 serve
+    FP32, TF32 and FP32_VIA_BF16, as on the device-timed leg).  The copy-in
+    stream, the compute stream and the copy-out stream are ordered by events,
+    so a buffer is only overwritten after every earlier use has finished."""
     import torch
     from accelerator_gb300 import binding, inputs
-    hA = torch.from_numpy(A).pin_memory()
-    hB = torch.from_numpy(B).pin_memory()
-    hA16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).pin_memory()
-    hB16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).pin_memory()
-    modes = {"fp32": (hA, hB, binding.FP32), "tf32": (hA, hB, binding.TF32),
-             "bf16": (hA16, hB16, binding.BF16), "fp32_via_bf16": (hA, hB, binding.FP32_VIA_BF16)}
-    if "fp16" in args.modes:
-        modes["fp16"] = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).pin_memory(),
-                         torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).pin_memory(), binding.FP16)
+    mode_ids = {"fp32": binding.FP32, "tf32": binding.TF32, "bf16": binding.BF16,
+                "fp16": binding.FP16, "fp32_via_bf16": binding.FP32_VIA_BF16}
+    # the input set each mode reads, and the host copies of each set
+    group_of = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "bf16": "bf16",
+                "fp16": "fp16"}
+    host = {}
+    for g in sorted({group_of[m] for m in args.modes}):
+        if g == "f32":
+            host[g] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), None)
+        elif g == "bf16":
+            host[g] = (torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).pin_memory(),
+                       torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).pin_memory(),
+                       torch.bfloat16)
+        else:
+            host[g] = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).pin_memory(),
+                       torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).pin_memory(),
+                       torch.float16)
     # two sets of device buffers, used by alternate steps, so that a step's
-    # copies need not wait for the previous step's product on the same mode
-    bufs = [{}, {}]
+    # copies need not wait for the previous step's products
+    ins, outs = [{}, {}], [{}, {}]
     for k in range(2):
+        for g, (ha, hb, view) in host.items():
+            ins[k][g] = dict(ha=ha, hb=hb, view=view,
+                             xa=torch.empty(ha.shape, dtype=ha.dtype, device=dev),
+                             xb=torch.empty(hb.shape, dtype=hb.dtype, device=dev),
+                             loaded=torch.cuda.Event(), readers=[])
         for m in args.modes:
-            ha, hb, mode = modes[m]
-            bufs[k][m] = dict(ha=ha, hb=hb, mode=mode,
-                              xa=torch.empty(ha.shape, dtype=ha.dtype, device=dev),
-                              xb=torch.empty(hb.shape, dtype=hb.dtype, device=dev),
-                              c=torch.empty((n, n), dtype=torch.float32, device=dev),
+            outs[k][m] = dict(c=torch.empty((n, n), dtype=torch.float32, device=dev),
                               hc=torch.empty((n, n), dtype=torch.float32).pin_memory(),
-                              loaded=torch.cuda.Event(), done=torch.cuda.Event(),
-                              out=torch.cuda.Event(), used=False)
-    h2d = sum(modes[m][0].numel() * modes[m][0].element_size() * 2 for m in args.modes)
+                              done=torch.cuda.Event(), out=torch.cuda.Event(), used=False)
+    h2d = sum(ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
+              for ha, hb, _ in host.values())
     d2h = len(args.modes) * n * n * 4
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     parity = [0]
 
     def e2e_step():
-        for m in args.modes:
-            b = bufs[parity[0]][m]
+        k = parity[0]
+        for g, b in ins[k].items():
             with torch.cuda.stream(s_in):
-                if b["used"]:
-                    s_in.wait_event(b["done"])      # the last product has read xa, xb
+                for ev in b["readers"]:
+                    s_in.wait_event(ev)                # the last products have read xa, xb
                 b["xa"].copy_(b["ha"], non_blocking=True)
                 b["xb"].copy_(b["hb"], non_blocking=True)
                 b["loaded"].record(s_in)
+            b["readers"] = []
+        for m in args.modes:
+            b, o = ins[k][group_of[m]], outs[k][m]
             stream.wait_event(b["loaded"])
-            if b["used"]:
-                stream.wait_event(b["out"])         # the last copy-out has read c
+            if o["used"]:
+                stream.wait_event(o["out"])             # the last copy-out has read c
             xa, xb = b["xa"], b["xb"]
-            if b["mode"] == binding.BF16:
-                xa, xb = xa.view(torch.bfloat16), xb.view(torch.bfloat16)
-            elif b["mode"] == binding.FP16:
-                xa, xb = xa.view(torch.float16), xb.view(torch.float16)
-            binding.gemm(xa, xb, b["c"], mode=b["mode"], stream=stream)
-            b["done"].record(stream)
+            if b["view"] is not None:
+                xa, xb = xa.view(b["view"]), xb.view(b["view"])
+            binding.gemm(xa, xb, o["c"], mode=mode_ids[m], stream=stream)
+            o["done"].record(stream)
+            b["readers"].append(o["done"])
             with torch.cuda.stream(s_out):
-                s_out.wait_event(b["done"])
-                b["hc"].copy_(b["c"], non_blocking=True)
-                b["out"].record(s_out)
-            b["used"] = True
+                s_out.wait_event(o["done"])
+                o["hc"].copy_(o["c"], non_blocking=True)
+                o["out"].record(s_out)
+            o["used"] = True
         parity[0] ^= 1
 
     for _ in range(2):
@@ -522,7 +537,8 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
         raise RuntimeError("a kernel reported a timeout during the end-to-end run")
     return {"value": ws * len(args.modes) * f / (ms / 1e3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "overlap": "copy-in, compute and copy-out on three streams"}
+            "overlap": "copy-in, compute and copy-out on three streams; each input copied "
+                       "once per step and shared by the modes that read it"}
 
 
 def _cpu_model() -> str:
