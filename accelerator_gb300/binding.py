@@ -23,6 +23,7 @@ ERR_NO_MEMORY = 4
 ERR_UNSUPPORTED_DEVICE = 5
 ERR_TIMEOUT = 6
 ERR_SCRATCH_LIMIT = 7
+ERR_BOUNDS = 8          # debug build only: an out-of-buffer access was caught and skipped
 
 # Every entry point include/gemm.h declares, with its ctypes signature.
 _i64, _vp, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -33,6 +34,7 @@ SIGNATURES = {
     "gemm_status_string": (ctypes.c_char_p, [_int]),
     "gemm_debug_status": (_int, [_vp]),
     "gemm_version": (_int, []),
+    "gemm_debug_build": (_int, []),
     "gemm_launch_count": (_i64, []),
     "gemm_selftest_bounded_wait": (_int, [_i64, _vp]),
     "gemm_tf32_noalloc": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
@@ -49,17 +51,24 @@ class GemmError(RuntimeError):
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded libgemm.so.  Raises if it has not been built."""
+    """The loaded libgemm.so.  Raises if it has not been built.
+
+    With LIBGEMM_DEBUG=1 in the environment (read at the first call) the debug
+    build is loaded instead: kernels with device-side bounds checks, built by
+    ``python -m accelerator_gb300.build --debug``.
+    """
     global _lib
     if _lib is not None:          # loaded: no lock needed to read it
         return _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            debug = os.environ.get("LIBGEMM_DEBUG", "") not in ("", "0")
+            path = _build.LIB_DEBUG if debug else _build.LIB
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"libgemm is not built ({path} missing); run "
-                    "`python -m accelerator_gb300.build` (or __graft_entry__.build())")
+                    "`python -m accelerator_gb300.build" + (" --debug" if debug else "")
+                    + "` (or __graft_entry__.build())")
             handle = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 f = getattr(handle, name)
@@ -154,6 +163,11 @@ def _operands(A, B, C, mode):
 
 def debug_status(stream=None) -> int:
     return int(lib().gemm_debug_status(_stream_ptr(stream) or None))
+
+
+def debug_build() -> bool:
+    """True when the loaded library carries the device-side bounds checks."""
+    return bool(lib().gemm_debug_build())
 
 
 def launch_count() -> int:

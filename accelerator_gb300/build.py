@@ -3,7 +3,12 @@
 One nvcc process per translation unit, run in parallel, then one link.  The
 CUDA runtime is linked statically; the driver's tensor-map encoder is looked up
 at run time, so the library loads (but cannot compute) on a machine without a
-GPU driver.  Usage: ``python -m accelerator_gb300.build [--verbose]``.
+GPU driver.  Usage: ``python -m accelerator_gb300.build [--verbose] [--debug]``.
+
+``--debug`` builds the debug variant into _build/debug/libgemm.so: the same
+sources compiled with GEMM_DEBUG, whose kernels check every global access
+against its buffer and report instead of touching memory outside it (the
+binding loads it when LIBGEMM_DEBUG=1).
 """
 from __future__ import annotations
 
@@ -19,6 +24,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgemm.so")
+BUILD_DEBUG = os.path.join(BUILD, "debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libgemm.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -41,22 +48,23 @@ def _deps():
         + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    out_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + (["-DGEMM_DEBUG=1"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -69,15 +77,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stderr.write(f"--- {os.path.basename(s)}\n{r.stdout}{r.stderr}")
     if failed:
         raise RuntimeError("nvcc failed for " + ", ".join(os.path.basename(s) for s, _ in failed))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("link of libgemm.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose="--verbose" in sys.argv))
+    print(build(force=True, verbose="--verbose" in sys.argv, debug="--debug" in sys.argv))

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "gemm.h"
+#include "debug.cuh"
 #include "kernels.h"
 
 namespace {
@@ -428,6 +429,7 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_NO_MEMORY: return "scratch allocation failed";
     case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
     case GEMM_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case GEMM_ERR_BOUNDS: return "a kernel access outside its buffer was detected and skipped (debug build)";
     case GEMM_ERR_SCRATCH_LIMIT:
         return "the product needs more scratch than the no-allocation entry point's static buffer";
     default: return "unknown status";
@@ -443,12 +445,16 @@ int gemm_debug_status(struct CUstream_st* stream_) {
     unsigned word = 0;
     if (cudaMemcpy(&word, st->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
         return GEMM_ERR_CUDA;
-    if (word == 0) return GEMM_OK;
+    // debug build: the bounds-check flags of every kernel (read and cleared)
+    const unsigned bounds = ffma_debug_flags() | tc_debug_flags() | prep_debug_flags();
+    if (word == 0) return bounds ? GEMM_ERR_BOUNDS : GEMM_OK;
     const unsigned zero = 0;
     if (cudaMemcpy(st->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_ERR_TIMEOUT;
 }
+
+int gemm_debug_build(void) { return kDebugBuild ? 1 : 0; }
 
 int gemm_version(void) { return 100; }
 

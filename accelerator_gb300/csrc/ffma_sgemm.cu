@@ -31,6 +31,7 @@
 //     handling of the first page's section 05, for any M, K, N.
 //   * Tiles are visited in groups of 8 tile-rows so CTAs running together
 //     share A and B slabs in L2.
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -97,6 +98,10 @@ struct SlabLoader {
     bool b_col_ok;
     int a_k, b_k;                      // this thread's k offset within a slab (A, B)
     uint32_t a_dst, b_dst;             // shared addresses in ring slot 0
+#ifdef GEMM_DEBUG
+    const float *dbg_a, *dbg_b;        // the operands and their sizes in bytes
+    int64_t dbg_a_bytes, dbg_b_bytes;
+#endif
 
     __device__ __forceinline__ SlabLoader(const float* A, const float* B, float* sA, float* sB,
                                           int M, int N, int K, int m0, int n0, int tid) {
@@ -116,6 +121,10 @@ struct SlabLoader {
         b_ptr = b_col_ok ? B + (int64_t)b_k * N + n0 + bc : B;
         n = N;
         b_dst = smem_u32(sB + b_k * kLdB + bc);
+#ifdef GEMM_DEBUG
+        dbg_a = A, dbg_b = B;
+        dbg_a_bytes = (int64_t)M * K * 4, dbg_b_bytes = (int64_t)K * N * 4;
+#endif
     }
 
     // Copies of slab kt into ring slot `slot` for a tile wholly inside M and N
@@ -129,7 +138,8 @@ struct SlabLoader {
             const float* row = a_ptr + j * a_group_step + k0;
 #pragma unroll
             for (int g = 0; g < kBK / 8; ++g)
-                cp_async_4(adst + (uint32_t)((8 * g * kLdA + kRowsPerPass * j) * 4), row + 8 * g);
+                if (GEMM_DBG_OK(row + 8 * g, dbg_a, dbg_a_bytes, 4))
+                    cp_async_4(adst + (uint32_t)((8 * g * kLdA + kRowsPerPass * j) * 4), row + 8 * g);
         }
         const uint32_t bdst = b_dst + (uint32_t)(slot * kBStage * 4);
         const float* bsrc = b_ptr + (int64_t)k0 * n;
@@ -137,6 +147,7 @@ struct SlabLoader {
         for (int r = 0; r < kBPer; ++r) {
             const float* src = bsrc + (int64_t)(kBRowsPerPass * r) * n;
             const uint32_t dst = bdst + (uint32_t)(kBRowsPerPass * r * kLdB * 4);
+            if (!GEMM_DBG_OK(src, dbg_b, dbg_b_bytes, 4 * kBElems)) continue;
             if constexpr (kBVec)
                 cp_async_16(dst, src);
             else
@@ -156,6 +167,7 @@ struct SlabLoader {
             bool ok = (a_row_ok >> j) & 1u;
             if (check_k) ok = ok && (kk + a_k < K);
             const float* src = ok ? a_ptr + j * a_group_step + kk : a_base;
+            if (ok) ok = GEMM_DBG_OK(src, dbg_a, dbg_a_bytes, 4);
             cp_async_4(adst + (uint32_t)((8 * g * kLdA + kRowsPerPass * j) * 4), src, ok);
         }
         const uint32_t bdst = b_dst + (uint32_t)(slot * kBStage * 4);
@@ -165,6 +177,7 @@ struct SlabLoader {
             bool ok = b_col_ok;
             if (check_k) ok = ok && (k0 + kBRowsPerPass * r + b_k < K);
             const float* src = ok ? bsrc + (int64_t)(kBRowsPerPass * r) * n : b_ptr;
+            if (ok) ok = GEMM_DBG_OK(src, dbg_b, dbg_b_bytes, 4 * kBElems);
             const uint32_t dst = bdst + (uint32_t)(kBRowsPerPass * r * kLdB * 4);
             if constexpr (kBVec)
                 cp_async_16(dst, src, ok);
@@ -301,15 +314,21 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
         // of the tile combine all of them.
         const int st = tile - dp_tiles;
         float* mine = partial + ((int64_t)st * splits + part) * (kBM * kBN);
+#ifdef GEMM_DEBUG
+        const int64_t part_bytes = (int64_t)(tiles_m * tiles_n - dp_tiles) * splits * (kBM * kBN) * 4;
+#endif
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int h = 0; h < TN / 4; ++h)
-                *reinterpret_cast<float4*>(mine + row_of(i) * kBN + col_of(4 * h)) =
-                    make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2), acc(i, 4 * h + 3));
+                if (GEMM_DBG_OK(mine + row_of(i) * kBN + col_of(4 * h), partial, part_bytes, 16))
+                    *reinterpret_cast<float4*>(mine + row_of(i) * kBN + col_of(4 * h)) =
+                        make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2), acc(i, 4 * h + 3));
         __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = atomicAdd(counters + st, 1u) == (unsigned)(splits - 1);
+        if (tid == 0)
+            s_last = GEMM_DBG_OK(counters + st, counters, (int64_t)(tiles_m * tiles_n - dp_tiles) * 4, 4) &&
+                     atomicAdd(counters + st, 1u) == (unsigned)(splits - 1);
         __syncthreads();
         if (!s_last) return;
         __threadfence();
@@ -319,6 +338,9 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
 #pragma unroll
             for (int h = 0; h < TN / 4; ++h) {
                 const int c = row_of(i) * kBN + col_of(4 * h);
+                if (!GEMM_DBG_OK(base + (int64_t)(splits - 1) * (kBM * kBN) + c, partial, part_bytes, 16) ||
+                    !GEMM_DBG_OK(base + c, partial, part_bytes, 16))
+                    continue;
                 float4 sum = __ldcg(reinterpret_cast<const float4*>(base + c));
                 for (int p = 1; p < splits; ++p) {
                     const float4 v = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)p * (kBM * kBN) + c));
@@ -340,6 +362,7 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
         for (int h = 0; h < TN / 4; ++h) {
             const int col = n0 + col_of(4 * h);
             if (kCVec && col < N) {   // N % 4 == 0: all four columns are in range
+                if (!GEMM_DBG_OK(crow + col, C, (int64_t)M * N * 4, 16)) continue;
                 *reinterpret_cast<float4*>(crow + col) = epilogue_apply4(
                     epi,
                     make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2),
@@ -348,7 +371,8 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (col + j < N) crow[col + j] = epilogue_apply(epi, acc(i, 4 * h + j), crow + col + j);
+                    if (col + j < N && GEMM_DBG_OK(crow + col + j, C, (int64_t)M * N * 4, 4))
+                        crow[col + j] = epilogue_apply(epi, acc(i, 4 * h + j), crow + col + j);
             }
         }
     }
@@ -476,5 +500,7 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
                                      sp, plan, partial, counters, ws, epi);
     return cudaGetLastError();
 }
+
+LIBGEMM_DEBUG_READER(ffma_debug_flags)
 
 }  // namespace libgemm

@@ -90,6 +90,12 @@ int tc_max_pairs();
 // the rest, and every unit has at least one), each storing its raw partial
 // as one 256 x 256 fp32 block of a workspace (block (tile - whole_tiles) *
 // splits + split), which launch_tc_tile_reduce adds up into C.
+// Bounds-check flags of each translation unit's kernels, read and cleared
+// (debug build; always 0 in the release build).
+unsigned ffma_debug_flags();
+unsigned tc_debug_flags();
+unsigned prep_debug_flags();
+
 struct TcSplit {
     int splits, k_per_split, whole_tiles;
 };

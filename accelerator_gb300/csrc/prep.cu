@@ -11,6 +11,7 @@
 //               show the bounded wait gives up and reports instead of hanging.
 #include <cuda_bf16.h>
 
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -25,7 +26,9 @@ __global__ void restride_kernel(const T* __restrict__ src, T* __restrict__ dst, 
         T* d = dst + r * dst_ld;
         for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
              c += (int64_t)gridDim.x * blockDim.x)
-            d[c] = s[c];
+            if (GEMM_DBG_OK(s + c, src, ((rows - 1) * src_ld + cols) * (int64_t)sizeof(T), sizeof(T)) &&
+                GEMM_DBG_OK(d + c, dst, rows * dst_ld * (int64_t)sizeof(T), sizeof(T)))
+                d[c] = s[c];
     }
 }
 
@@ -42,13 +45,15 @@ __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst,
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
             const int64_t r = r0 + ty + j, c = c0 + tx;
-            if (r < rows && c < cols) tile[ty + j][tx] = src[r * cols + c];
+            if (r < rows && c < cols && GEMM_DBG_OK(src + r * cols + c, src, rows * cols * (int64_t)sizeof(T), sizeof(T)))
+                tile[ty + j][tx] = src[r * cols + c];
         }
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
             const int64_t c = c0 + ty + j, r = r0 + tx;   // dst row c, column r
-            if (r < rows && c < cols) dst[c * dst_ld + r] = tile[tx][ty + j];
+            if (r < rows && c < cols && GEMM_DBG_OK(dst + c * dst_ld + r, dst, cols * dst_ld * (int64_t)sizeof(T), sizeof(T)))
+                dst[c * dst_ld + r] = tile[tx][ty + j];
         }
         __syncthreads();
     }
@@ -76,7 +81,9 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int64_t r = r0 + t / 16 + 16 * p, c4 = c0 / 4 + t % 16;
-            w[p] = (r < rows && c4 < cols4) ? src[r * cols4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            w[p] = (r < rows && c4 < cols4 && GEMM_DBG_OK(src + r * cols4 + c4, src, rows * cols4 * 16, 16))
+                       ? src[r * cols4 + c4]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     int64_t tl = blockIdx.x;
@@ -96,7 +103,7 @@ __global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restr
         for (int p = 0; p < 4; ++p) {
             const int dr = t / 16 + 16 * p, dk = 4 * (t % 16);
             const int64_t row = c0 + dr, k = r0 + dk;
-            if (row < cols && k < rows)
+            if (row < cols && k < rows && GEMM_DBG_OK(dst + row * dst_ld + k, dst, cols * dst_ld * 4, 16))
                 *reinterpret_cast<float4*>(dst + row * dst_ld + k) =
                     make_float4(tile[dk][dr], tile[dk + 1][dr], tile[dk + 2][dr], tile[dk + 3][dr]);
         }
@@ -112,6 +119,9 @@ __global__ void to_bf16_v4_kernel(const float4* __restrict__ src, uint2* __restr
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
         for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols4;
              c += (int64_t)gridDim.x * blockDim.x) {
+            if (!GEMM_DBG_OK(src + r * cols4 + c, src, rows * cols4 * 16, 16) ||
+                !GEMM_DBG_OK(dst + r * dst_ld4 + c, dst, rows * dst_ld4 * 8, 8))
+                continue;
             const float4 v = src[r * cols4 + c];
             const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
@@ -145,12 +155,14 @@ __global__ void __launch_bounds__(256) to_bf16_pair_kernel(Bf16Job a, Bf16Job b)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t c = c0 + q * (int64_t)blockDim.x;
-                v[q] = c < j.cols4 ? __ldcs(s + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[q] = c < j.cols4 && GEMM_DBG_OK(s + c, j.src, j.rows * j.cols4 * 16, 16)
+                           ? __ldcs(s + c)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t c = c0 + q * (int64_t)blockDim.x;
-                if (c < j.cols4) {
+                if (c < j.cols4 && GEMM_DBG_OK(d + c, j.dst, j.rows * j.dst_ld4 * 8, 8)) {
                     const __nv_bfloat162 lo = __floats2bfloat162_rn(v[q].x, v[q].y);
                     const __nv_bfloat162 hi = __floats2bfloat162_rn(v[q].z, v[q].w);
                     d[c] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
@@ -166,20 +178,22 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __r
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
         for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
              c += (int64_t)gridDim.x * blockDim.x)
-            dst[r * dst_ld + c] = __float2bfloat16_rn(src[r * cols + c]);
+            if (GEMM_DBG_OK(src + r * cols + c, src, rows * cols * 4, 4) &&
+                GEMM_DBG_OK(dst + r * dst_ld + c, dst, rows * dst_ld * 2, 2))
+                dst[r * dst_ld + c] = __float2bfloat16_rn(src[r * cols + c]);
 }
 
 __global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
-        C[i] = 0.0f;
+        if (GEMM_DBG_OK(C + i, C, n * 4, 4)) C[i] = 0.0f;
 }
 
 // C := beta * C, one rounding per element (alpha == 0 or K == 0 with beta != 0).
 __global__ void scale_kernel(float* __restrict__ C, int64_t n, float beta) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
-        C[i] = __fmul_rn(beta, C[i]);
+        if (GEMM_DBG_OK(C + i, C, n * 4, 4)) C[i] = __fmul_rn(beta, C[i]);
 }
 
 // K-split fix-up: C_ij := epilogue(p_0 + p_1 + ... + p_{S-1}), the partials
@@ -200,6 +214,10 @@ __global__ void __launch_bounds__(256)
          u += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = u / nw, j = (u - i * nw) * W;
         const float* p = ws + i * ws_ld + j;
+        if (!GEMM_DBG_OK(p, ws, splits * sstride * 4, 4 * W) ||
+            !GEMM_DBG_OK(p + (splits - 1) * sstride, ws, splits * sstride * 4, 4 * W) ||
+            !GEMM_DBG_OK(C + i * N + j, C, M * N * 4, 4 * W))
+            continue;
         if constexpr (kVec) {
             float4 acc = __ldcg(reinterpret_cast<const float4*>(p));
             int s = 1;
@@ -391,5 +409,7 @@ cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t 
     wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
     return cudaGetLastError();
 }
+
+LIBGEMM_DEBUG_READER(prep_debug_flags)
 
 }  // namespace libgemm

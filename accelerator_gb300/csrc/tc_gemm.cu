@@ -38,6 +38,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -102,13 +103,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
 // M x N (16 bytes at a time when vec: C rows 16-byte aligned); values outside
 // are never stored.
 __device__ __forceinline__ void epilogue_row32(const Epilogue& e, uint32_t (&v)[32],
-                                               const float* crow, int row, int col0, int M,
-                                               int N, bool vec) {
+                                               const float* crow, const float* C, int row,
+                                               int col0, int M, int N, bool vec) {
     if (e.kind == 0) return;
     if (e.kind == 2 && row < M) {
         if (vec && col0 + 32 <= N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
+                if (!GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 16)) continue;
                 const float4 r = epilogue_apply4(
                     e,
                     make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
@@ -120,7 +122,7 @@ __device__ __forceinline__ void epilogue_row32(const Epilogue& e, uint32_t (&v)[
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < N)
+                if (col0 + j < N && GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 4))
                     v[j] = __float_as_uint(epilogue_apply(e, __uint_as_float(v[j]), crow + col0 + j));
         }
         return;
@@ -290,18 +292,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
-                epilogue_row32(epi, v, crow, row, col0, M, N, c_vec != 0);
+                epilogue_row32(epi, v, crow, C, row, col0, M, N, c_vec != 0);
                 if (row < M) {
                     if (c_vec && col0 + 32 <= N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(crow + col0 + j) =
-                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                            if (GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 16))
+                                *reinterpret_cast<float4*>(crow + col0 + j) =
+                                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                            if (col0 + j < N && GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 4))
+                                crow[col0 + j] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
-                if (!to_ws) epilogue_row32(epi, v, crow, row, col0, M, N, c_mode != kStoreScalar);
+                if (!to_ws) epilogue_row32(epi, v, crow, C, row, col0, M, N, c_mode != kStoreScalar);
                 if (mode_u == kStoreTma) {
                     // Stage the warp's 32 x 32 block (row = lane) with the 128-byte
                     // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then
@@ -606,13 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (mode_u == kStoreVec && col0 + 32 <= N) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(crow + col0 + j) =
-                                make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                            __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                            if (GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 16))
+                                *reinterpret_cast<float4*>(crow + col0 + j) =
+                                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(v[j]);
+                            if (col0 + j < N && GEMM_DBG_OK(crow + col0 + j, C, (int64_t)M * N * 4, 4))
+                                crow[col0 + j] = __uint_as_float(v[j]);
                     }
                 }
             }
@@ -657,6 +663,9 @@ __global__ void __launch_bounds__(256)
         const int i = m0 + r, j = n0 + 4 * c4;
         if (i >= M || j >= N) continue;
         const float* p = ws + ((int64_t)t * splits * kTile + r) * kTile + 4 * c4;
+        const int64_t ws_bytes = (int64_t)split_tiles * splits * kBlock * 4;
+        if (!GEMM_DBG_OK(p, ws, ws_bytes, 16) || !GEMM_DBG_OK(p + (splits - 1) * kBlock, ws, ws_bytes, 16))
+            continue;
         float4 acc = __ldcg(reinterpret_cast<const float4*>(p));
         int sp = 1;
         for (; sp + 4 <= splits; sp += 4) {
@@ -673,6 +682,7 @@ __global__ void __launch_bounds__(256)
             acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
         }
         float* c = C + (int64_t)i * N + j;
+        if (!GEMM_DBG_OK(c, C, (int64_t)M * N * 4, c_vec ? 16 : 4)) continue;
         if (c_vec) {   // N % 4 == 0: the four columns are inside C
             *reinterpret_cast<float4*>(c) = epilogue_apply4(epi, acc, c);
         } else {
@@ -913,5 +923,7 @@ cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a
 #undef LIBGEMM_TC_LAUNCH
     return cudaGetLastError();
 }
+
+LIBGEMM_DEBUG_READER(tc_debug_flags)
 
 }  // namespace libgemm

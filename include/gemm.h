@@ -80,8 +80,12 @@ enum gemm_status {
     GEMM_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 */
     GEMM_ERR_TIMEOUT = 6,            /* a bounded wait inside a kernel expired; the kernel
                                         stopped early and its output is not valid */
-    GEMM_ERR_SCRATCH_LIMIT = 7       /* gemm_tf32_noalloc: the product needs more scratch
+    GEMM_ERR_SCRATCH_LIMIT = 7,      /* gemm_tf32_noalloc: the product needs more scratch
                                         than GEMM_NOALLOC_SCRATCH_BYTES */
+    GEMM_ERR_BOUNDS = 8              /* debug build only (gemm_debug_build() == 1): a kernel
+                                        computed a global-memory access outside the buffer
+                                        it belongs to; the access was skipped and the
+                                        output is not valid */
 };
 
 /*
@@ -132,10 +136,21 @@ GEMM_API const char* gemm_status_string(int status);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word, which kernels set when a bounded wait expires.  Returns GEMM_OK,
- * GEMM_ERR_TIMEOUT, or GEMM_ERR_CUDA if the synchronisation itself failed.
+ * word, which kernels set when a bounded wait expires, and, in the debug
+ * build, the bounds-check flags.  Returns GEMM_OK, GEMM_ERR_TIMEOUT,
+ * GEMM_ERR_BOUNDS (debug build; a timeout is reported first when both
+ * happened), or GEMM_ERR_CUDA if the synchronisation itself failed.
  */
 GEMM_API int gemm_debug_status(struct CUstream_st* stream);
+
+/*
+ * 1 when this library was built with device-side bounds checks (compiled
+ * with GEMM_DEBUG: every kernel checks each global access against the extent
+ * of the buffer it belongs to, skips one that falls outside and records it
+ * for gemm_debug_status), 0 for the release build, whose kernels carry no
+ * checks.  The checks stand in for a memory checker where none can run.
+ */
+GEMM_API int gemm_debug_build(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 GEMM_API int gemm_version(void);

@@ -50,3 +50,21 @@ def assert_exact(C, Cref, what=""):
         bad = np.argwhere(C != Cref)[:5]
         raise AssertionError(f"{what}: {int((C != Cref).sum())} entries differ, e.g. "
                              f"{[(tuple(i), C[tuple(i)], Cref[tuple(i)]) for i in bad]}")
+
+
+U = 2.0 ** -24   # unit roundoff of binary32
+
+
+def assert_update_within(out, P, S, C_in, alpha, beta, tol, what):
+    """|out - (alpha P + beta C_in)| <= |alpha| tol S plus the epilogue's own
+    two roundings, 2u (|alpha| S + |beta C_in|) (|P| <= S)."""
+    import oracle
+    ref = oracle.update(P, C_in, alpha, beta)
+    out = np.asarray(out, np.float64)
+    assert np.all(np.isfinite(out)), f"{what}: non-finite entries"
+    c_abs = 0.0 if C_in is None else np.abs(C_in)
+    lim = abs(alpha) * tol * S + 2 * U * (abs(alpha) * S + abs(beta) * c_abs) + 1e-30
+    err = np.abs(out - ref)
+    bad = err > lim
+    assert not bad.any(), (f"{what}: {int(bad.sum())} entries off, e.g. "
+                           f"{[(tuple(i), out[tuple(i)], ref[tuple(i)]) for i in np.argwhere(bad)[:4]]}")

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from accelerator_gb300 import inputs
-from checks import TOL
+from checks import TOL, assert_update_within
 from gpu_util import device_operands, oracle_inputs, run
 
 pytestmark = pytest.mark.gpu
@@ -22,7 +22,6 @@ pytestmark = pytest.mark.gpu
 MODES = ["fp32", "tf32", "bf16", "fp16", "fp32_via_bf16"]
 SHAPES = [(300, 200, 520), (257, 130, 261)]
 SCALARS = [(1.0, 0.0), (2.5, 0.0), (-0.75, 1.5), (1.0, 1.0), (0.0, -2.0), (0.0, 0.0), (0.0, 1.0)]
-U = 2.0 ** -24
 
 
 def run_ex(binding, A, B, C_in, alpha, beta, mode):
@@ -34,20 +33,6 @@ def run_ex(binding, A, B, C_in, alpha, beta, mode):
     torch.cuda.synchronize()
     assert binding.debug_status() == binding.OK
     return c.cpu().numpy()
-
-
-def assert_update_within(out, P, S, C_in, alpha, beta, tol, what):
-    """|out - (alpha P + beta C_in)| <= |alpha| tol S plus the epilogue's own
-    two roundings, 2u (|alpha| S + |beta C_in|) (|P| <= S)."""
-    ref = oracle.update(P, C_in, alpha, beta)
-    out = np.asarray(out, np.float64)
-    assert np.all(np.isfinite(out)), f"{what}: non-finite entries"
-    c_abs = 0.0 if C_in is None else np.abs(C_in)
-    lim = abs(alpha) * tol * S + 2 * U * (abs(alpha) * S + abs(beta) * c_abs) + 1e-30
-    err = np.abs(out - ref)
-    bad = err > lim
-    assert not bad.any(), (f"{what}: {int(bad.sum())} entries off, e.g. "
-                           f"{[(tuple(i), out[tuple(i)], ref[tuple(i)]) for i in np.argwhere(bad)[:4]]}")
 
 
 @pytest.mark.parametrize("mode", MODES)
