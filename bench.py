@@ -463,8 +463,10 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     # the input set each mode reads, and the host copies of each set
     group_of = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "bf16": "bf16",
                 "fp16": "fp16"}
+    # copied in the order the step's products first read them, so that the
+    # first product waits only for its own inputs
     host = {}
-    for g in sorted({group_of[m] for m in args.modes}):
+    for g in dict.fromkeys(group_of[m] for m in args.modes):
         if g == "f32":
             host[g] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), None)
         elif g == "bf16":
