@@ -122,6 +122,13 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
               const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
     const bool b_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+    if (ffma_small_fits(M, N, K, st->num_sms)) {   // small product: 32 x 32 tiles, one launch
+        if (launch_ffma_small(A, B, C, (int)M, (int)N, (int)K, b_vec, c_vec, epi, stream) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_launches++;
+        return GEMM_OK;
+    }
     const FfmaPlan plan = ffma_plan((int)M, (int)N, (int)K, st->num_sms);
     void* scratch = nullptr;
     float* partial = nullptr;
@@ -446,7 +453,8 @@ int gemm_debug_status(struct CUstream_st* stream_) {
     if (cudaMemcpy(&word, st->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
         return GEMM_ERR_CUDA;
     // debug build: the bounds-check flags of every kernel (read and cleared)
-    const unsigned bounds = ffma_debug_flags() | tc_debug_flags() | prep_debug_flags();
+    const unsigned bounds =
+        ffma_debug_flags() | ffma_small_debug_flags() | tc_debug_flags() | prep_debug_flags();
     if (word == 0) return bounds ? GEMM_ERR_BOUNDS : GEMM_OK;
     const unsigned zero = 0;
     if (cudaMemcpy(st->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)

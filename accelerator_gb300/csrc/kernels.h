@@ -68,6 +68,17 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
                               unsigned* counters, const Epilogue& epi, float* ws,
                               cudaStream_t stream);
 
+// ---- small-product FFMA GEMM (ffma_small.cu) ----
+// Products with at most kSmallMaxMN outputs and K <= kSmallMaxK take the
+// 32 x 32-tile kernel (one launch, no K split); GEMM_FORCE_CONFIG=ffma_small
+// or =ffma_tiles128 makes every FP32 product take one of the two kernels
+// (testing and tuning only).
+constexpr int64_t kSmallMaxMN = 384 * 384, kSmallMaxK = 512;
+bool ffma_small_fits(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_ffma_small(const float* A, const float* B, float* C, int M, int N, int K,
+                              bool b_vec, bool c_vec, const Epilogue& epi, cudaStream_t stream);
+unsigned ffma_small_debug_flags();
+
 // ---- tcgen05 tensor-core GEMM (tc_gemm.cu) ----
 enum class TcMode { kBF16, kTF32, kF16 };
 struct TcShape {
