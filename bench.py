@@ -448,6 +448,27 @@ def run_libgemm(args):
     return 0
 
 
+# The input set each mode reads on the end-to-end leg: A and B as float32
+# serve FP32, TF32 and FP32_VIA_BF16; bfloat16 and binary16 copies serve the
+# others.  Bytes per element of each set.
+E2E_GROUP_OF = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "bf16": "bf16",
+                "fp16": "fp16"}
+E2E_GROUP_BYTES = {"f32": 4, "bf16": 2, "fp16": 2}
+
+
+def e2e_input_groups(modes):
+    """The input sets a step copies, once each, in the order its products
+    first read them (so the first product waits only for its own inputs)."""
+    return list(dict.fromkeys(E2E_GROUP_OF[m] for m in modes))
+
+
+def e2e_bytes_per_step(modes, n):
+    """(host-to-device, device-to-host) bytes of one end-to-end step of
+    square n x n products: A and B of every input set in, every C out."""
+    h2d = sum(2 * n * n * E2E_GROUP_BYTES[g] for g in e2e_input_groups(modes))
+    return h2d, len(modes) * n * n * 4
+
+
 def run_e2e(args, A, B, n, dev, stream, ws, f):
     """E2E throughput: per step, the H2D copies of the step's inputs from
     pinned host memory, one product per mode, and the D2H copy of every
@@ -460,13 +481,9 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     from accelerator_gb300 import binding, inputs
     mode_ids = {"fp32": binding.FP32, "tf32": binding.TF32, "bf16": binding.BF16,
                 "fp16": binding.FP16, "fp32_via_bf16": binding.FP32_VIA_BF16}
-    # the input set each mode reads, and the host copies of each set
-    group_of = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "bf16": "bf16",
-                "fp16": "fp16"}
-    # copied in the order the step's products first read them, so that the
-    # first product waits only for its own inputs
+    group_of = E2E_GROUP_OF
     host = {}
-    for g in dict.fromkeys(group_of[m] for m in args.modes):
+    for g in e2e_input_groups(args.modes):
         if g == "f32":
             host[g] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), None)
         elif g == "bf16":
@@ -493,6 +510,7 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     h2d = sum(ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
               for ha, hb, _ in host.values())
     d2h = len(args.modes) * n * n * 4
+    assert (h2d, d2h) == e2e_bytes_per_step(args.modes, n)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     parity = [0]
 

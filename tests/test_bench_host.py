@@ -40,3 +40,16 @@ def test_mode_selection():
     assert bench.ALL_MODES[:3] == bench.MODES == ("fp32", "tf32", "bf16")
     # every selectable mode has a stated nominal peak or the FFMA peak formula
     assert all(m in bench.NOMINAL_TFLOPS for m in bench.ALL_MODES if m != "fp32")
+
+
+def test_e2e_input_sets():
+    # FP32 and TF32 read the same float32 A and B: the default step copies
+    # two input sets, float32 first because the FP32 product runs first
+    assert bench.e2e_input_groups(bench.MODES) == ["f32", "bf16"]
+    assert bench.e2e_input_groups(("bf16", "fp32")) == ["bf16", "f32"]
+    assert bench.e2e_input_groups(bench.ALL_MODES) == ["f32", "bf16", "fp16"]
+    assert bench.e2e_input_groups(("tf32", "fp32_via_bf16")) == ["f32"]
+    # 4096^2: 2 x 64 MiB float32 + 2 x 32 MiB bfloat16 in, 3 x 64 MiB out
+    h2d, d2h = bench.e2e_bytes_per_step(bench.MODES, 4096)
+    assert h2d == 201326592 and d2h == 201326592
+    assert set(bench.E2E_GROUP_OF) == set(bench.ALL_MODES)
