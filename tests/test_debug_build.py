@@ -7,9 +7,9 @@ CPU: both variants build and say which they are.  GPU: a child process loads
 the debug build and runs products along every kernel path -- FFMA interior
 and edge tiles, the in-kernel split of a partial last wave and the workspace
 split, the tensor kernels whole, with the last round split and all split,
-the 1-SM fallback, the re-stride, transpose and conversion passes, the alpha
-/ beta update and K = 0 -- each checked against the oracle, with no bounds
-report after any of them."""
+the 1-SM fallback, the small-product FFMA kernel, the re-stride, transpose
+and conversion passes, the alpha / beta update and K = 0 -- each checked
+against the oracle, with no bounds report after any of them."""
 import ctypes
 import os
 import subprocess
@@ -79,8 +79,10 @@ if single:
         check(mode, 256, 8192, 256)
 else:
     # FFMA: workspace split (few tiles), scalar B and C (N % 4 != 0), interior
-    # tiles only, a partial last wave split in the kernel, alpha / beta
-    for shp in [(1000, 777, 1500), (300, 700, 201), (2048, 64, 2048)]:
+    # tiles only, a partial last wave split in the kernel, alpha / beta; the
+    # 32 x 32-tile kernel of small products (vector and scalar forms)
+    for shp in [(1000, 777, 1500), (300, 700, 201), (2048, 64, 2048), (200, 136, 264),
+                (31, 500, 33)]:
         check("fp32", *shp)
     check("fp32", 2816, 256, 2816, sampled=True)
     check("fp32", 1000, 777, 1500, alpha=0.5, beta=-1.25)
@@ -115,7 +117,7 @@ def _child(env_extra):
 @pytest.mark.gpu
 def test_debug_build_all_paths_in_bounds():
     out = _child({})
-    assert out.count("ok ") == 26
+    assert out.count("ok ") == 28
 
 
 @pytest.mark.gpu
