@@ -61,11 +61,10 @@ struct Cfg {
     static_assert(kWarpsM * kWarpsN * 32 == kThreads, "warps cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "4 x 4 sub-blocks");
 };
-// 8 x 8 per thread, 256 threads, lanes 8 (M) x 4 (N).
-using Cfg8x8 = Cfg<8, 8, 8, 4, false, 256, 4, 2>;
 // 16 x 8 per thread, 128 threads, lanes 4 (M) x 8 (N) with N fastest: a
 // quarter-warp shares one A chunk, so 6 fragment loads per k cost 16
-// wavefronts for 128 FMAs (the 8 x 8 layout: 12 for 64).
+// wavefronts for 128 FMAs (an 8 x 8 layout with lanes 8 (M) x 4 (N): 12 for
+// 64; measured 19 % slower at 4096^3).
 using Cfg16x8 = Cfg<16, 8, 4, 8, true, 128, 3, 3>;
 using FfmaCfg = Cfg16x8;
 
