@@ -10,13 +10,22 @@ the split really is taken (two kernels for an aligned BF16 product).  The
 FP32 (FFMA) path splits shapes with very few tiles the same way ("wide"
 split: every tile cut into up to 256 K ranges, partials added by the same
 second kernel); it is covered by the same checks.
+
+Each check can see a split piece dropped or added twice: where the oracle
+is given the values the tensor cores read (TF32-truncated, bfloat16,
+binary16), only the binary32 accumulation may differ, so the same-inputs
+tolerance (1e-4 S) applies, well below one piece's share at any K here; and
+integer inputs in [-4, 4] (every partial an integer below 2**24, exact in
+any order) are compared bit for bit, in every mode, at the three split
+regimes: one pair tile in 74 pieces (256 x 65536 x 256), four pair tiles
+(1024 x 16384 x 1024), and the last partial round of 4096^3.
 """
 import numpy as np
 import pytest
 
 import oracle
 from accelerator_gb300 import inputs
-from checks import TOL, assert_within
+from checks import TOL, TOL_SAME_INPUTS, assert_exact, assert_within
 from gpu_util import device_operands, oracle_inputs, run
 
 pytestmark = pytest.mark.gpu
@@ -24,16 +33,23 @@ pytestmark = pytest.mark.gpu
 TC_MODES = ["tf32", "bf16", "fp16"]
 
 
+def _same_inputs(A, B, mode):
+    """(A, B, fmt, tol): the oracle's operands as the kernels read them, and
+    the tolerance of the binary32 accumulation alone."""
+    Ao, Bo, fmt = oracle_inputs(A, B, "bf16" if mode == "fp32_via_bf16" else mode)
+    return Ao, Bo, fmt, min(TOL[mode], TOL_SAME_INPUTS)
+
+
 def _sampled(libgemm, M, K, N, mode, dist="pm1", n=2048):
     A, B = inputs.matrices(M, K, N, dist, seed=M + K + N)
     C = run(libgemm, A, B, mode)
-    Ao, Bo, fmt = oracle_inputs(A, B, mode)
+    Ao, Bo, fmt, tol = _same_inputs(A, B, mode)
     rows, cols = inputs.sample_indices(M, N, n)
     Cref, S = oracle.dot(Ao, Bo, rows, cols, fmt)
-    assert_within(C[rows, cols], Cref, S, TOL[mode], f"{mode} {M}x{K}x{N}")
+    assert_within(C[rows, cols], Cref, S, tol, f"{mode} {M}x{K}x{N}")
     tot, atot = oracle.total(Ao, Bo, fmt)
     got = float(np.sum(C.astype(np.float64)))
-    assert abs(got - tot) <= TOL[mode] * atot, (got, tot)
+    assert abs(got - tot) <= tol * atot, (got, tot)
     return A, B, C
 
 
@@ -53,12 +69,36 @@ def test_fp32_wide_split(libgemm, M, K, N):
 def test_ragged_split_full(libgemm, mode, M, K, N):
     A, B = inputs.matrices(M, K, N, "pm1", seed=M * 3 + N)
     C = run(libgemm, A, B, mode)
-    if mode == "fp32_via_bf16":
-        Ao, Bo, fmt = A, B, "f32"
-    else:
-        Ao, Bo, fmt = oracle_inputs(A, B, mode)
+    Ao, Bo, fmt, tol = _same_inputs(A, B, mode)
     Cref, S = oracle.gemm(Ao, Bo, fmt)
-    assert_within(C, Cref, S, TOL[mode], f"{mode} {M}x{K}x{N}")
+    assert_within(C, Cref, S, tol, f"{mode} {M}x{K}x{N}")
+    # and against the original float32 values at the mode's own tolerance
+    Cref, S = oracle.gemm(A, B)
+    assert_within(C, Cref, S, TOL[mode], f"{mode} {M}x{K}x{N} (f32 inputs)")
+
+
+ALL_MODES = ["tf32", "bf16", "fp16", "fp32", "fp32_via_bf16"]
+
+
+@pytest.mark.parametrize("mode", ALL_MODES)
+@pytest.mark.parametrize("M,K,N", [(256, 65536, 256), (1024, 16384, 1024), (4096, 4096, 4096)])
+def test_integers_bit_exact_at_each_split_regime(libgemm, mode, M, K, N):
+    """|C| <= 16 K <= 2**20: every partial is an integer, exact in any order,
+    so the split result must equal the oracle's bit for bit.  Full C for the
+    single-tile split; sampled entries plus the exact sum of all entries for
+    the larger shapes (a missing or doubled piece moves the sum)."""
+    A, B = inputs.matrices(M, K, N, "int4", seed=M + K + N)
+    C = run(libgemm, A, B, mode)
+    what = f"{mode} int {M}x{K}x{N}"
+    if M * N <= 256 * 256:
+        Cref, _ = oracle.gemm(A, B)
+        assert_exact(C, Cref, what)
+    else:
+        rows, cols = inputs.sample_indices(M, N, 4096)
+        Cref, _ = oracle.dot(A, B, rows, cols)
+        assert_exact(C[rows, cols], Cref, what + " sampled")
+    tot, _ = oracle.total(A, B)
+    assert float(np.sum(C.astype(np.float64))) == tot, what + " sum of all entries"
 
 
 @pytest.mark.parametrize("mode", ["bf16", "tf32", "fp32"])
