@@ -103,15 +103,17 @@ bool ranges_overlap(uintptr_t a, uint64_t abytes, uintptr_t b, uint64_t bbytes) 
 }
 
 // 2-D tensor map over a rows x cols row-major matrix with row stride ld
-// (elements), box box_cols x box_rows, 128-byte swizzle, zero fill outside.
+// (elements), box box_cols x box_rows, 128-byte swizzle (of 16-byte chunks,
+// or of 32-byte chunks for an MN-major TF32 operand), zero fill outside.
 int encode_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols, int64_t ld,
-              int box_cols, int box_rows, CUtensorMapDataType dt) {
+              int box_cols, int box_rows, CUtensorMapDataType dt,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -180,144 +182,89 @@ CUtensorMapDataType tensor_type(TcMode mode) {
                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// K-split product: the pair kernel computes the whole tiles into C (with
-// the epilogue) and stores the split units' raw partials as 256 x 256 blocks
-// of a workspace from the pool; the reduce kernel adds each split tile's
-// blocks in split order, applies the epilogue and writes C.
-int split_tc_launch(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
-                    const CUtensorMap& map_b, const CUtensorMap* map_c, float* C, int64_t M,
-                    int64_t K, int64_t N, bool c_vec, const Epilogue& epi, const TcSplit& split,
-                    DeviceState* st, cudaStream_t stream) {
-    const int64_t bytes = tc_split_workspace_bytes(split, M, N);
-    void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, (size_t)bytes, st->pool, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_NO_MEMORY;
-    }
-    CUtensorMap map_w;
-    int rc = encode_2d(&map_w, ws, 4, bytes / (256 * 4), 256, 256, 32, 32,
-                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
-    if (rc == GEMM_OK) {
-        if (launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, map_c, &map_w, C, (int)M, (int)N,
-                                (int)K, c_vec, epi, split, st->err, kWaitLimitNs, stream) !=
-            cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        else
-            g_launches++;
-    }
-    if (rc == GEMM_OK) {
-        if (launch_tc_tile_reduce(static_cast<const float*>(ws), split, C, (int)M, (int)N, c_vec,
-                                  epi, st->num_sms, stream) != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        else
-            g_launches++;
-    }
-    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
-    return rc;
-}
-
 // The product on operands TMA can read: A (M x K, row stride lda) and B
-// (K x N, stride ldb) or, with b_k_major, B^T (N x K, stride ldb), with
-// 16-byte aligned bases and strides.
-int tc_launch(TcMode mode, bool b_k_major, const void* a_use, int64_t lda, const void* b_use,
-              int64_t ldb, float* C, int64_t M, int64_t K, int64_t N, const Epilogue& epi,
-              DeviceState* st, cudaStream_t stream) {
+// (K x N, row stride ldb), 16-byte aligned bases and strides.  With a K
+// split (split.splits > 1) the pair kernel computes the whole tiles into C
+// and stores the split units' raw partials as 256 x 256 blocks of the
+// workspace ws; the reduce kernel then adds each split tile's blocks in
+// split order, applies the epilogue and writes C.
+int tc_launch(TcMode mode, const void* a_use, int64_t lda, const void* b_use, int64_t ldb,
+              float* C, int64_t M, int64_t K, int64_t N, const Epilogue& epi,
+              const TcSplit& split, void* ws, DeviceState* st, cudaStream_t stream) {
     const int es = mode == TcMode::kTF32 ? 4 : 2;
     const CUtensorMapDataType dt = tensor_type(mode);
     const TcShape shape = tc_shape(mode);
-    // The 2-SM kernel (CTA pairs) when the device can hold pair clusters; each
-    // CTA of a pair loads half of the B tile, so a K-major B box is half as tall.
+    // the 2-SM kernel (CTA pairs) when the device can hold pair clusters
     const bool pairs = tc_max_pairs() > 0;
-    const int b_rows = pairs ? shape.block_n / 2 : shape.block_n;
     CUtensorMap map_a, map_b;
     int rc = encode_2d(&map_a, a_use, es, M, K, lda, shape.k_elems, shape.block_m, dt);
+    // An MN-major B of 32-bit elements lands in the 128-byte swizzle of
+    // 32-byte chunks, the layout kind::tf32 reads such an operand in.
+    const CUtensorMapSwizzle b_swizzle =
+        es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
     if (rc == GEMM_OK)
-        rc = b_k_major ? encode_2d(&map_b, b_use, es, N, K, ldb, shape.k_elems, b_rows, dt)
-                       : encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt);
+        rc = encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt, b_swizzle);
+    if (rc != GEMM_OK) return rc;
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
     // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
     CUtensorMap map_c;
-    const bool c_tma = pairs && c_vec && rc == GEMM_OK &&
+    const bool c_tma = pairs && c_vec &&
                        encode_2d(&map_c, C, 4, M, N, N, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) == GEMM_OK;
-    const TcSplit split = pairs && rc == GEMM_OK ? tc_plan_split(mode, M, N, K) : kNoSplit;
-    if (rc == GEMM_OK && split.splits > 1)
-        return split_tc_launch(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr, C, M, K, N,
-                               c_vec, epi, split, st, stream);
-    if (rc == GEMM_OK) {
-        const cudaError_t e =
-            pairs ? launch_tc_gemm_pair(mode, b_k_major, map_a, map_b, c_tma ? &map_c : nullptr,
-                                        nullptr, C, (int)M, (int)N, (int)K, c_vec, epi, kNoSplit,
-                                        st->err, kWaitLimitNs, stream)
-                  : launch_tc_gemm(mode, b_k_major, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec,
-                                   epi, st->num_sms, st->err, kWaitLimitNs, stream);
-        if (e != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        else
-            g_launches++;
+    const CUtensorMap* mc = c_tma ? &map_c : nullptr;
+    if (split.splits > 1) {
+        if (!pairs || !ws) return GEMM_ERR_INVALID_ARG;
+        const int64_t bytes = tc_split_workspace_bytes(split, M, N);
+        CUtensorMap map_w;
+        rc = encode_2d(&map_w, ws, 4, bytes / (256 * 4), 256, 256, 32, 32,
+                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+        if (rc != GEMM_OK) return rc;
+        if (launch_tc_gemm_pair(mode, map_a, map_b, mc, &map_w, C, (int)M, (int)N, (int)K, c_vec,
+                                epi, split, st->err, kWaitLimitNs, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_launches++;
+        if (launch_tc_tile_reduce(static_cast<const float*>(ws), split, C, (int)M, (int)N, c_vec,
+                                  epi, st->num_sms, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_launches++;
+        return GEMM_OK;
     }
-    return rc;
+    const cudaError_t e =
+        pairs ? launch_tc_gemm_pair(mode, map_a, map_b, mc, nullptr, C, (int)M, (int)N, (int)K,
+                                    c_vec, epi, kNoSplit, st->err, kWaitLimitNs, stream)
+              : launch_tc_gemm(mode, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec, epi,
+                               st->num_sms, st->err, kWaitLimitNs, stream);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    g_launches++;
+    return GEMM_OK;
 }
 
 int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_t M, int64_t K,
                      int64_t N, const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
-    const int es = mode == TcMode::kTF32 ? 4 : 2;
-    const int64_t align_elems = 16 / es;
-    // BF16 reads B as an MN-major operand, straight from the caller's K x N
-    // rows.  The MN-major form of kind::tf32 returned zeros on GB300, so the
-    // TF32 kernel reads B^T (N x K, K-major), made by a transpose pass.
-    const bool b_k_major = mode == TcMode::kTF32;
-    // TMA wants 16-byte aligned bases and row strides that are multiples of 16 bytes.
-    const bool pad_a = (K % align_elems) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
-    const bool pad_b = !b_k_major &&
-                       ((N % align_elems) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0);
-    const int64_t lda = pad_a ? round_up(K, align_elems) : K;
-    const int64_t ldb = b_k_major ? round_up(K, align_elems) : (pad_b ? round_up(N, align_elems) : N);
-    const int64_t a_bytes = pad_a ? round_up(M * lda * es, 256) : 0;
-    const int64_t b_bytes = b_k_major ? round_up(N * ldb * es, 256) : (pad_b ? round_up(K * ldb * es, 256) : 0);
-
+    const TcPlan plan = tc_plan(mode, A, B, M, K, N);
     void* scratch = nullptr;
-    const void* a_use = A;
-    const void* b_use = B;
-    if (a_bytes + b_bytes > 0) {
-        if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes), st->pool, stream) !=
+    if (plan.scratch_bytes() > 0 &&
+        cudaMallocFromPoolAsync(&scratch, (size_t)plan.scratch_bytes(), st->pool, stream) !=
             cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_NO_MEMORY;
-        }
-        uint8_t* s = static_cast<uint8_t*>(scratch);
-        int rc = GEMM_OK;
-        if (pad_a) {
-            if (launch_restride(A, s, M, K, K, lda, es, stream) != cudaSuccess) rc = GEMM_ERR_CUDA;
-            g_launches++;
-            a_use = s;
-        }
-        if (rc == GEMM_OK && b_bytes > 0) {
-            cudaError_t e = b_k_major ? launch_transpose(B, s + a_bytes, K, N, ldb, es, st->num_sms, stream)
-                                      : launch_restride(B, s + a_bytes, K, N, N, ldb, es, stream);
-            if (e != cudaSuccess) rc = GEMM_ERR_CUDA;
-            g_launches++;
-            b_use = s + a_bytes;
-        }
-        if (rc != GEMM_OK) {
-            cudaFreeAsync(scratch, stream);
-            return rc;
-        }
+        cudaGetLastError();
+        return GEMM_ERR_NO_MEMORY;
     }
-
-    int rc = tc_launch(mode, b_k_major, a_use, lda, b_use, ldb, C, M, K, N, epi, st, stream);
+    int rc = tc_product(plan, A, B, C, M, K, N, epi, scratch, stream);
     if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }
 
 // GEMM_FP32_VIA_BF16: round A and B to bfloat16 into scratch rows whose
-// stride is a multiple of 16 bytes (TMA-ready), then the BF16 product.
+// stride is a multiple of 16 bytes (TMA-ready), then the BF16 product
+// (with the split workspace, when the product is split, after them).
 int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
                       const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
     const int64_t lda = round_up(K, 8), ldb = round_up(N, 8);
     const int64_t a_bytes = round_up(M * lda * 2, 256), b_bytes = round_up(K * ldb * 2, 256);
+    const TcSplit split = tc_plan_split(TcMode::kBF16, M, N, K);
+    const int64_t ws_bytes = round_up(tc_split_workspace_bytes(split, M, N), 256);
     void* scratch = nullptr;
-    if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes), st->pool, stream) !=
-        cudaSuccess) {
+    if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes + ws_bytes), st->pool,
+                                stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_NO_MEMORY;
     }
@@ -328,7 +275,8 @@ int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64
         rc = GEMM_ERR_CUDA;
     g_launches += launched;
     if (rc == GEMM_OK)
-        rc = tc_launch(TcMode::kBF16, false, s, lda, s + a_bytes, ldb, C, M, K, N, epi, st, stream);
+        rc = tc_launch(TcMode::kBF16, s, lda, s + a_bytes, ldb, C, M, K, N, epi, split,
+                       ws_bytes ? s + a_bytes + b_bytes : nullptr, st, stream);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }
@@ -348,10 +296,49 @@ int device_setup(int* num_sms, unsigned** err) {
     return GEMM_OK;
 }
 
-int encode_tensor_map_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols,
-                         int64_t ld, int box_cols, int box_rows) {
-    return encode_2d(map, ptr, es, rows, cols, ld, box_cols, box_rows,
-                     es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+TcPlan tc_plan(TcMode mode, const void* A, const void* B, int64_t M, int64_t K, int64_t N) {
+    const int es = mode == TcMode::kTF32 ? 4 : 2;
+    const int64_t align_elems = 16 / es;
+    TcPlan p;
+    p.mode = mode;
+    // TMA wants 16-byte aligned bases and row strides that are multiples of
+    // 16 bytes; an operand that has neither is copied with a padded stride.
+    // B is read as the caller stores it (K x N rows, MN-major) in every mode.
+    p.pad_a = (K % align_elems) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
+    p.pad_b = (N % align_elems) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
+    p.lda = p.pad_a ? round_up(K, align_elems) : K;
+    p.ldb = p.pad_b ? round_up(N, align_elems) : N;
+    p.a_bytes = p.pad_a ? round_up(M * p.lda * es, 256) : 0;
+    p.b_bytes = p.pad_b ? round_up(K * p.ldb * es, 256) : 0;
+    p.split = tc_plan_split(mode, M, N, K);
+    p.ws_bytes = round_up(tc_split_workspace_bytes(p.split, M, N), 256);
+    return p;
+}
+
+int tc_product(const TcPlan& plan, const void* A, const void* B, float* C, int64_t M, int64_t K,
+               int64_t N, const Epilogue& epi, void* scratch, cudaStream_t stream) {
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != GEMM_OK) return rc;
+    if (plan.scratch_bytes() > 0 && !scratch) return GEMM_ERR_INVALID_ARG;
+    const int es = plan.mode == TcMode::kTF32 ? 4 : 2;
+    uint8_t* s = static_cast<uint8_t*>(scratch);
+    const void* a_use = A;
+    const void* b_use = B;
+    if (plan.pad_a) {
+        if (launch_restride(A, s, M, K, K, plan.lda, es, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        g_launches++;
+        a_use = s;
+    }
+    if (plan.pad_b) {
+        if (launch_restride(B, s + plan.a_bytes, K, N, N, plan.ldb, es, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        g_launches++;
+        b_use = s + plan.a_bytes;
+    }
+    void* ws = plan.ws_bytes ? s + plan.a_bytes + plan.b_bytes : nullptr;
+    return tc_launch(plan.mode, a_use, plan.lda, b_use, plan.ldb, C, M, K, N, epi, plan.split, ws,
+                     st, stream);
 }
 
 void count_launch() { g_launches++; }

@@ -90,9 +90,10 @@ TcShape tc_shape(TcMode mode);
 cudaError_t tc_setup();
 // Clusters of two CTAs of the 2-SM kernel that fit at once (0: unavailable).
 int tc_max_pairs();
-// 2-SM (CTA pair) kernel: BF16 with B MN-major, or TF32 with B^T K-major.
-// Its TMA boxes: A as for the 1-SM kernel; B boxes of k_elems rows x 128
-// bytes (MN-major) or 128 rows x 128 bytes (K-major), i.e. block_n / 2 wide.
+// 2-SM (CTA pair) kernel, B read MN-major in every mode.  Its TMA boxes: A
+// as for the 1-SM kernel (block_m rows x 128 bytes); B boxes of k_elems rows
+// x 128 bytes (b_box_n columns), 128-byte swizzle of 16-byte chunks for
+// 16-bit elements and of 32-byte chunks for TF32.
 // map_c (may be null): C as a 2-D fp32 tensor, box 32 x 32, 128-byte swizzle,
 // for TMA stores of the epilogue; without it C is stored by the threads.
 // K split of the pair kernel: the first whole_tiles pair tiles (in the
@@ -118,7 +119,7 @@ TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K);
 int64_t tc_split_workspace_bytes(const TcSplit& split, int64_t M, int64_t N);
 // map_w (needed when split.splits > 1): the workspace as a 2-D fp32 tensor of
 // 256 columns, row stride 256, box 32 x 32, 128-byte swizzle.
-cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+cudaError_t launch_tc_gemm_pair(TcMode mode, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c,
                                 const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
                                 const Epilogue& epi, const TcSplit& split, unsigned* err,
@@ -132,8 +133,8 @@ cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t ws_rows, int64_t ws_ld,
                                  float* C, int64_t M, int64_t N, bool c_vec, const Epilogue& epi,
                                  int num_sms, cudaStream_t stream);
-// b_k_major: map_b describes B^T (N x K, K contiguous) instead of B (K x N).
-cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+// 1-SM kernel (128 x 256 tiles), the fallback where pair clusters do not fit.
+cudaError_t launch_tc_gemm(TcMode mode, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
                            const Epilogue& epi, int num_sms, unsigned* err, uint64_t limit_ns,
                            cudaStream_t stream);
@@ -143,9 +144,6 @@ cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a
 // row stride dst_ld (both in elements).
 cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t cols,
                             int64_t src_ld, int64_t dst_ld, int es, cudaStream_t stream);
-// dst (cols x rows, row stride dst_ld elements) = transpose of src (rows x cols, dense).
-cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
-                             int64_t dst_ld, int es, int num_sms, cudaStream_t stream);
 // dst (rows x cols bfloat16, row stride dst_ld elements) = round-to-nearest-
 // even of src (rows x cols float, dense).
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t cols,
@@ -165,10 +163,26 @@ cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t 
 // Per-device set-up of the library (device check, kernel attributes, error
 // word); returns a gemm_status code.
 int device_setup(int* num_sms, unsigned** err);
-// Tensor map over a rows x cols row-major matrix (row stride ld elements),
-// box box_cols x box_rows, 128-byte swizzle, zero fill; gemm_status code.
-int encode_tensor_map_2d(CUtensorMap* map, const void* ptr, int es, int64_t rows, int64_t cols,
-                         int64_t ld, int box_cols, int box_rows);
+// How a tensor-core product (TF32, BF16, FP16 mode) runs: the row strides
+// its kernels read A and B with, the K split, and the device scratch that
+// takes, as one block [re-strided A | re-strided B | split workspace], each
+// part a multiple of 256 bytes.  gemm() takes the block from its memory
+// pool; gemm_tf32_noalloc() from its static buffer.
+struct TcPlan {
+    TcMode mode;
+    bool pad_a, pad_b;            // operand copied into scratch with a 16-byte row stride
+    int64_t lda, ldb;             // row strides (elements) the kernels read A and B with
+    int64_t a_bytes, b_bytes;     // scratch for the copies (0: read in place)
+    TcSplit split;
+    int64_t ws_bytes;             // split workspace (0: the product is not split)
+    int64_t scratch_bytes() const { return a_bytes + b_bytes + ws_bytes; }
+};
+TcPlan tc_plan(TcMode mode, const void* A, const void* B, int64_t M, int64_t K, int64_t N);
+// Enqueues a planned product (K > 0) on `stream`; scratch: plan.scratch_bytes()
+// bytes of device memory, 256-byte aligned (may be null when that is 0).
+// Returns a gemm_status code.
+int tc_product(const TcPlan& plan, const void* A, const void* B, float* C, int64_t M, int64_t K,
+               int64_t N, const Epilogue& epi, void* scratch, cudaStream_t stream);
 // Add one to the library's launch counter.
 void count_launch();
 

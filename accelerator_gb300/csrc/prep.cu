@@ -32,85 +32,6 @@ __global__ void restride_kernel(const T* __restrict__ src, T* __restrict__ dst, 
     }
 }
 
-// 32 x 32 tiles through shared memory (one padding column keeps the
-// column-wise reads free of bank conflicts), so reads and writes are both
-// coalesced along rows.
-template <typename T>
-__global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
-                                 int64_t cols, int64_t dst_ld) {
-    __shared__ T tile[32][33];
-    const int tx = threadIdx.x, ty = threadIdx.y;   // block 32 x 8
-    const int64_t c0 = (int64_t)blockIdx.x * 32;
-    for (int64_t r0 = (int64_t)blockIdx.y * 32; r0 < rows; r0 += (int64_t)gridDim.y * 32) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            const int64_t r = r0 + ty + j, c = c0 + tx;
-            if (r < rows && c < cols && GEMM_DBG_OK(src + r * cols + c, src, rows * cols * (int64_t)sizeof(T), sizeof(T)))
-                tile[ty + j][tx] = src[r * cols + c];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            const int64_t c = c0 + ty + j, r = r0 + tx;   // dst row c, column r
-            if (r < rows && c < cols && GEMM_DBG_OK(dst + c * dst_ld + r, dst, cols * dst_ld * (int64_t)sizeof(T), sizeof(T)))
-                dst[c * dst_ld + r] = tile[tx][ty + j];
-        }
-        __syncthreads();
-    }
-}
-
-// Vector form for 32-bit elements when B's rows are 16-byte aligned
-// (cols % 4 == 0, 16-byte aligned base) and dst_ld % 4 == 0: 64 x 64 tiles,
-// every global access 16 bytes wide.  Persistent blocks walk the tiles; the
-// loads of a block's next tile are issued before it writes out the current
-// one, so they are in flight during the writes (one tile per block left
-// each block's loads exposed, and a partial last wave).  Rows
-// beyond `rows` read as zero; dst columns up to roundup(rows, 4) are written
-// (the padding is inside dst's row stride and is never read as data).
-__global__ void __launch_bounds__(256) transpose_v4_kernel(const float4* __restrict__ src,
-                                                           float* __restrict__ dst, int64_t rows,
-                                                           int64_t cols, int64_t dst_ld) {
-    __shared__ float tile[64][65];
-    grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
-    const int t = threadIdx.x;
-    const int64_t tiles_c = (cols + 63) / 64, tiles_r = (rows + 63) / 64;
-    const int64_t ntiles = tiles_c * tiles_r, cols4 = cols / 4;
-    float4 v[4];
-    auto load = [&](int64_t tl, float4 (&w)[4]) {
-        const int64_t c0 = (tl % tiles_c) * 64, r0 = (tl / tiles_c) * 64;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int64_t r = r0 + t / 16 + 16 * p, c4 = c0 / 4 + t % 16;
-            w[p] = (r < rows && c4 < cols4 && GEMM_DBG_OK(src + r * cols4 + c4, src, rows * cols4 * 16, 16))
-                       ? src[r * cols4 + c4]
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    int64_t tl = blockIdx.x;
-    if (tl < ntiles) load(tl, v);
-    for (; tl < ntiles; tl += gridDim.x) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int rr = t / 16 + 16 * p, cc = 4 * (t % 16);
-            tile[rr][cc] = v[p].x, tile[rr][cc + 1] = v[p].y;
-            tile[rr][cc + 2] = v[p].z, tile[rr][cc + 3] = v[p].w;
-        }
-        __syncthreads();
-        const int64_t next = tl + gridDim.x;
-        if (next < ntiles) load(next, v);   // in flight while this tile is written out
-        const int64_t c0 = (tl % tiles_c) * 64, r0 = (tl / tiles_c) * 64;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int dr = t / 16 + 16 * p, dk = 4 * (t % 16);
-            const int64_t row = c0 + dr, k = r0 + dk;
-            if (row < cols && k < rows && GEMM_DBG_OK(dst + row * dst_ld + k, dst, cols * dst_ld * 4, 16))
-                *reinterpret_cast<float4*>(dst + row * dst_ld + k) =
-                    make_float4(tile[dk][dr], tile[dk + 1][dr], tile[dk + 2][dr], tile[dk + 3][dr]);
-        }
-        __syncthreads();
-    }
-}
-
 // float -> bfloat16, round to nearest even, into rows of stride dst_ld.  The
 // vector form reads 4 floats (16 bytes) and writes 4 bf16 (8 bytes) per step;
 // it needs cols % 4 == 0, 16-byte aligned src and 8-byte aligned dst rows.
@@ -283,32 +204,6 @@ cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t co
     else if (es == 2)
         restride_kernel<uint16_t><<<grid, threads, 0, stream>>>(
             static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, src_ld, dst_ld);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols,
-                             int64_t dst_ld, int es, int num_sms, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    if (es == 4 && cols % 4 == 0 && dst_ld % 4 == 0 &&
-        (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-        const int64_t ntiles = ((cols + 63) / 64) * ((rows + 63) / 64);
-        const int64_t cap = (int64_t)num_sms * 8;   // persistent: 8 resident blocks per SM
-        const unsigned vgrid = (unsigned)(ntiles < cap ? ntiles : cap);
-        transpose_v4_kernel<<<vgrid, 256, 0, stream>>>(static_cast<const float4*>(src),
-                                                       static_cast<float*>(dst), rows, cols, dst_ld);
-        return cudaGetLastError();
-    }
-    const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
-    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535)), block(32, 8);
-    if (es == 4)
-        transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, dst_ld);
-    else if (es == 2)
-        transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, dst_ld);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

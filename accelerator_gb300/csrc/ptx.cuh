@@ -322,21 +322,28 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uin
     }
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+// Shared-memory matrix descriptor for tcgen05.mma.
 //   bits  0-13  start address >> 4
 //   bits 16-29  leading-dimension byte offset >> 4
 //   bits 32-45  stride-dimension byte offset >> 4
 //   bits 46-48  fixed value 0b001
 //   bits 49-51  base offset (0: every tile starts on a 1024-byte boundary)
-//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+//   bits 61-63  layout (swizzle) type: 2 = 128-byte swizzle of 16-byte
+//               chunks; 1 = 128-byte swizzle of 32-byte chunks, the form an
+//               MN-major operand of 32-bit (TF32) elements takes
+enum : uint32_t { kLayoutSw128Atom32 = 1, kLayoutSw128 = 2 };
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(addr, lbo, sbo, kLayoutSw128);
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32 with an F32 accumulator.

@@ -1,4 +1,4 @@
-// tc_gemm.cu -- tensor-core GEMM on sm_103a (modes GEMM_TF32 and GEMM_BF16).
+// tc_gemm.cu -- tensor-core GEMM on sm_103a (modes GEMM_TF32, GEMM_BF16, GEMM_FP16).
 //
 // C_ij = sum_k A_ik B_kj ("Shared Memory Tiling for Matrix Multiplication",
 // opening formula), A M x K row-major (K-major), B K x N row-major (N-major),
@@ -29,8 +29,11 @@
 //     k-th MMA of a slab starts 32*k bytes into the rows.
 //   B slab: 128/es columns of N per 128-byte row, one row per k, boxes of
 //     128/es columns side by side every (K rows * 128) bytes: the canonical
-//     MN-major layout with leading byte offset = box size, stride byte
-//     offset = 1024 (8 k-rows).  The k-th MMA starts k*UMMA_K rows down.
+//     MN-major layout with leading byte offset = box size.  16-bit elements:
+//     16-byte swizzle chunks, stride byte offset 1024 (8 k-rows); 32-bit
+//     (TF32) elements: 32-byte swizzle chunks, stride byte offset 512 (4
+//     k-rows).  The k-th MMA starts k*UMMA_K rows down.  B is read as the
+//     caller stores it (K x N rows) in every mode.
 //
 // Every wait is bounded (see mbar_wait): if one expires the CTA records a
 // timeout in the device error word, the roles stop, in-flight copies and
@@ -64,18 +67,28 @@ struct Traits<TcMode::kBF16> {
     static constexpr int kEs = 2;
     static constexpr uint32_t kFormat = 1;       // BF16
     static constexpr TcKind kKind = TcKind::kF16;
+    // MN-major B: 128-byte swizzle of 16-byte chunks, repeating every 8
+    // k-rows (1024 bytes), the stride byte offset between 8-row groups.
+    static constexpr uint32_t kBMnLayout = kLayoutSw128, kBMnSbo = 1024;
 };
 template <>
 struct Traits<TcMode::kF16> {
     static constexpr int kEs = 2;
     static constexpr uint32_t kFormat = 0;       // F16
     static constexpr TcKind kKind = TcKind::kF16;
+    static constexpr uint32_t kBMnLayout = kLayoutSw128, kBMnSbo = 1024;
 };
 template <>
 struct Traits<TcMode::kTF32> {
     static constexpr int kEs = 4;
     static constexpr uint32_t kFormat = 2;       // TF32
     static constexpr TcKind kKind = TcKind::kTF32;
+    // An MN-major operand of 32-bit elements is read in the 128-byte swizzle
+    // of 32-byte chunks (what the TMA writes with
+    // CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B), whose pattern repeats every 4
+    // k-rows: 512 bytes between 4-row groups.  (With the 16-byte-chunk
+    // swizzle an MN-major kind::tf32 operand reads as zeros.)
+    static constexpr uint32_t kBMnLayout = kLayoutSw128Atom32, kBMnSbo = 512;
 };
 
 struct Sched {
@@ -131,7 +144,7 @@ __device__ __forceinline__ void epilogue_row32(const Epilogue& e, uint32_t (&v)[
     for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__fmul_rn(e.alpha, __uint_as_float(v[j])));
 }
 
-template <TcMode MODE, bool kBKMajor>
+template <TcMode MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, float* __restrict__ C, int M, int N,
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBoxN = kSlabBytes / T::kEs;            // N per B box: 64 / 32
     constexpr int kBoxes = kBN / kBoxN;                   // 4 / 8
     constexpr uint32_t kBoxBytes = kKElems * kSlabBytes;  // 8 KB / 4 KB
-    constexpr uint32_t kIdesc = make_idesc(T::kFormat, kBM, kBN, false, !kBKMajor);
+    constexpr uint32_t kIdesc = make_idesc(T::kFormat, kBM, kBN, false, true);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -209,15 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_arrive_expect_tx(fb, kStageBytes);
                     tma_load_2d(sA + stage * kABytes, &map_a, fb, kb * kKElems, m0);
-                    if constexpr (kBKMajor) {
-                        // B^T (N x K, K contiguous): one box of kBN rows x 128 bytes
-                        tma_load_2d(sB + stage * kBBytes, &map_b, fb, kb * kKElems, n0);
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < kBoxes; ++j)
-                            tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, &map_b, fb,
-                                        n0 + j * kBoxN, kb * kKElems);
-                    }
+                    for (int j = 0; j < kBoxes; ++j)
+                        tma_load_2d(sB + stage * kBBytes + j * kBoxBytes, &map_b, fb,
+                                    n0 + j * kBoxN, kb * kKElems);
                     used[stage] = true;
                     last_phase[stage] = phase;
                     if (++stage == kStages) stage = 0, phase ^= 1u;
@@ -253,9 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kMmaPerStage; ++kk) {
                         const uint64_t adesc = smem_desc_sw128(a_tile + kk * 32, 16, 1024);
-                        const uint64_t bdesc =
-                            kBKMajor ? smem_desc_sw128(b_tile + kk * 32, 16, 1024)
-                                     : smem_desc_sw128(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes, 1024);
+                        const uint64_t bdesc = smem_desc(b_tile + kk * kUmmaK * kSlabBytes,
+                                                         kBoxBytes, T::kBMnSbo, T::kBMnLayout);
                         tc_mma<T::kKind>(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8 * stage);   // slot is free once these MMAs are done
@@ -373,7 +380,7 @@ constexpr int kPStageCBytes = 4 * 2 * 32 * 32 * 4;   // 32 KB
 constexpr size_t kPSmemBytes =
     size_t(kPStages) * kPStageBytes + kPStageCBytes + 1024 + 256;
 
-template <TcMode MODE, bool kBKMajor>
+template <TcMode MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBoxN = kSlabBytes / T::kEs;            // N per MN-major B box: 64 (bf16)
     constexpr int kBoxes = kPHalfN / kBoxN;               // 2 (bf16)
     constexpr uint32_t kBoxBytes = kKElems * kSlabBytes;  // 8 KB (bf16)
-    constexpr uint32_t kIdesc = make_idesc(T::kFormat, 2 * kBM, kBN, false, !kBKMajor);
+    constexpr uint32_t kIdesc = make_idesc(T::kFormat, 2 * kBM, kBN, false, true);
     constexpr uint32_t kPairTx = 2u * kPStageBytes;       // bytes the leader's full barrier awaits
 
     extern __shared__ uint8_t smem_raw[];
@@ -486,14 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, kPairTx);
                     const uint32_t fb = full_leader0 + 8 * stage;
                     tma_load_2d_pair(sA + stage * kPABytes, &map_a, fb, kb * kKElems, my_m0);
-                    if constexpr (kBKMajor) {
-                        tma_load_2d_pair(sB + stage * kPBBytes, &map_b, fb, kb * kKElems, my_n0);
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < kBoxes; ++j)
-                            tma_load_2d_pair(sB + stage * kPBBytes + j * kBoxBytes, &map_b, fb,
-                                             my_n0 + j * kBoxN, kb * kKElems);
-                    }
+                    for (int j = 0; j < kBoxes; ++j)
+                        tma_load_2d_pair(sB + stage * kPBBytes + j * kBoxBytes, &map_b, fb,
+                                         my_n0 + j * kBoxN, kb * kKElems);
                     used[stage] = true;
                     last_phase[stage] = phase;
                     if (++stage == kPStages) stage = 0, phase ^= 1u;
@@ -535,9 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kMmaPerStage; ++kk) {
                         const uint64_t adesc = smem_desc_sw128(a_tile + kk * 32, 16, 1024);
-                        const uint64_t bdesc =
-                            kBKMajor ? smem_desc_sw128(b_tile + kk * 32, 16, 1024)
-                                     : smem_desc_sw128(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes, 1024);
+                        const uint64_t bdesc = smem_desc(b_tile + kk * kUmmaK * kSlabBytes,
+                                                         kBoxBytes, T::kBMnSbo, T::kBMnLayout);
                         tc_mma_pair<T::kKind>(d_tmem, adesc, bdesc, kIdesc,
                                               (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
@@ -701,22 +703,22 @@ TcShape tc_shape(TcMode mode) {
     return TcShape{kBM, kBN, kSlabBytes / es, kSlabBytes / es};
 }
 
-template <TcMode MODE, bool BK>
+template <TcMode MODE>
 static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(tc_gemm_kernel<MODE, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes);
 }
 
-template <TcMode MODE, bool BK>
+template <TcMode MODE>
 static cudaError_t set_pair_attr() {
-    return cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE, BK>,
+    return cudaFuncSetAttribute(tc_gemm_pair_kernel<MODE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
 }
 
 // Clusters of two that can be resident at once (0: pairs unavailable).
 static int g_max_pairs = 0;
 
-template <TcMode MODE, bool BK>
+template <TcMode MODE>
 static int query_max_pairs(int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms & ~1));
@@ -730,7 +732,7 @@ static int query_max_pairs(int num_sms) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<MODE, BK>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -739,19 +741,17 @@ static int query_max_pairs(int num_sms) {
 
 cudaError_t tc_setup() {
     cudaError_t e;
-    if ((e = set_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
-    if ((e = set_attr<TcMode::kBF16, true>()) != cudaSuccess) return e;
-    if ((e = set_attr<TcMode::kTF32, false>()) != cudaSuccess) return e;
-    if ((e = set_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
-    if ((e = set_attr<TcMode::kF16, false>()) != cudaSuccess) return e;
-    if ((e = set_pair_attr<TcMode::kBF16, false>()) != cudaSuccess) return e;
-    if ((e = set_pair_attr<TcMode::kF16, false>()) != cudaSuccess) return e;
-    if ((e = set_pair_attr<TcMode::kTF32, true>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kBF16>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kTF32>()) != cudaSuccess) return e;
+    if ((e = set_attr<TcMode::kF16>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kBF16>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kF16>()) != cudaSuccess) return e;
+    if ((e = set_pair_attr<TcMode::kTF32>()) != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int a = query_max_pairs<TcMode::kBF16, false>(sms);
-    const int b = query_max_pairs<TcMode::kTF32, true>(sms);
+    const int a = query_max_pairs<TcMode::kBF16>(sms);
+    const int b = query_max_pairs<TcMode::kTF32>(sms);
     g_max_pairs = a < b ? a : b;
     // GEMM_FORCE_CONFIG=single_cta: use the 1-SM kernel even where pairs fit
     // (it is otherwise only taken on devices that cannot hold pair clusters).
@@ -814,7 +814,7 @@ TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K) {
     return plan;
 }
 
-cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+cudaError_t launch_tc_gemm_pair(TcMode mode, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c,
                                 const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
                                 const Epilogue& epi, const TcSplit& split, unsigned* err,
@@ -851,17 +851,15 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, bool b_k_major, const CUtensorMap& 
     const CUtensorMap& mw = map_w ? *map_w : map_a;   // unused without split units
     const int kps = splitting ? split.k_per_split : 0, wt = (int)whole;
     cudaError_t e;
-    if (mode == TcMode::kBF16 && !b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16, false>, map_a, map_b, mc, mw,
-                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
-    else if (mode == TcMode::kTF32 && b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32, true>, map_a, map_b, mc, mw,
-                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
-    else if (mode == TcMode::kF16 && !b_k_major)
-        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16, false>, map_a, map_b, mc, mw,
-                               C, M, N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
+    if (mode == TcMode::kBF16)
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16>, map_a, map_b, mc, mw, C, M,
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
+    else if (mode == TcMode::kTF32)
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32>, map_a, map_b, mc, mw, C, M,
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
     else
-        return cudaErrorInvalidValue;
+        e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16>, map_a, map_b, mc, mw, C, M,
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -897,7 +895,7 @@ cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* 
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a,
+cudaError_t launch_tc_gemm(TcMode mode, const CUtensorMap& map_a,
                            const CUtensorMap& map_b, float* C, int M, int N, int K, bool c_vec,
                            const Epilogue& epi, int num_sms, unsigned* err, uint64_t limit_ns,
                            cudaStream_t stream) {
@@ -907,19 +905,15 @@ cudaError_t launch_tc_gemm(TcMode mode, bool b_k_major, const CUtensorMap& map_a
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const int grid = (int)(tiles < num_sms ? tiles : num_sms);
     const int cv = c_vec ? 1 : 0;
-#define LIBGEMM_TC_LAUNCH(MODE_, BK_)                                                         \
-    tc_gemm_kernel<MODE_, BK_><<<grid, kThreads, kSmemBytes, stream>>>(                      \
-        map_a, map_b, C, M, N, K, tiles_m, tiles_n, cv, epi, err, limit_ns)
-    if (mode == TcMode::kBF16) {
-        if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kBF16, true);
-        else LIBGEMM_TC_LAUNCH(TcMode::kBF16, false);
-    } else if (mode == TcMode::kF16) {
-        if (b_k_major) return cudaErrorInvalidValue;
-        LIBGEMM_TC_LAUNCH(TcMode::kF16, false);
-    } else {
-        if (b_k_major) LIBGEMM_TC_LAUNCH(TcMode::kTF32, true);
-        else LIBGEMM_TC_LAUNCH(TcMode::kTF32, false);
-    }
+#define LIBGEMM_TC_LAUNCH(MODE_)                                                              \
+    tc_gemm_kernel<MODE_><<<grid, kThreads, kSmemBytes, stream>>>(map_a, map_b, C, M, N, K, tiles_m, \
+                                                                  tiles_n, cv, epi, err, limit_ns)
+    if (mode == TcMode::kBF16)
+        LIBGEMM_TC_LAUNCH(TcMode::kBF16);
+    else if (mode == TcMode::kF16)
+        LIBGEMM_TC_LAUNCH(TcMode::kF16);
+    else
+        LIBGEMM_TC_LAUNCH(TcMode::kTF32);
 #undef LIBGEMM_TC_LAUNCH
     return cudaGetLastError();
 }

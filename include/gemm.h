@@ -182,36 +182,49 @@ GEMM_API int gemm_selftest_bounded_wait(int64_t timeout_ns, struct CUstream_st* 
  * gemm_tf32_noalloc -- the GEMM_TF32 product without allocating device memory.
  *
  * The pages have no counterpart for this entry point; it is a service of this
- * library.  gemm() in GEMM_TF32 needs scratch (a transposed copy of B, and a
- * re-strided copy of A when A's rows are not 16-byte multiples) and takes it
- * from CUDA's stream-ordered allocator.  Some callers cannot allow that: a
- * host application that has reserved the device memory for its own pool, so
- * an allocation would fail or eat into its budget; or a latency-critical
- * loop where an allocation may stall or fail at a bad moment.  This entry
- * point uses instead one static device buffer of GEMM_NOALLOC_SCRATCH_BYTES,
- * compiled into the library: it never calls cudaMalloc, cudaMallocAsync,
- * cudaFree or any allocating routine.
+ * library.  gemm() in GEMM_TF32 sometimes needs scratch memory -- a copy of A
+ * or B with 16-byte row strides when TMA cannot read them in place (K or N
+ * not a multiple of 4, or a base not 16-byte aligned), and the workspace of
+ * a K split (products with few output tiles and a long K, or a partial last
+ * round of tiles, e.g. 4096^3) -- and takes it from CUDA's stream-ordered
+ * allocator.  Some callers cannot allow that: a host application that has
+ * reserved the device memory for its own pool, so an allocation would fail
+ * or eat into its budget; or a latency-critical loop where an allocation may
+ * stall or fail at a bad moment.  This entry point uses instead one static
+ * device buffer of GEMM_NOALLOC_SCRATCH_BYTES, compiled into the library: it
+ * never calls cudaMalloc, cudaMallocAsync, cudaFree or any allocating
+ * routine.
  *
  * Arguments and results are those of gemm() with precision_mode GEMM_TF32:
- * A, B, C device pointers (float), row-major, C overwritten, asynchronous on
- * `stream`, the same kernels and therefore the same values as gemm().
+ * A, B, C device pointers (float, 4-byte aligned), row-major, C overwritten,
+ * asynchronous on `stream`.  The product is planned exactly as gemm() plans
+ * it (the same kernels, the same K split, the same order of summation), so
+ * C equals gemm()'s C bit for bit.  K == 0 gives C = 0.
  *
- * Limit: 4 * N * roundup(K, 4) bytes (rounded up to 256) for B^T, plus, when A
- * is not 16-byte aligned or K % 4 != 0, 4 * M * roundup(K, 4) bytes (rounded
- * up to 256) for A, must not exceed GEMM_NOALLOC_SCRATCH_BYTES (64 MiB: for
- * example K = N = 4096 with an aligned A).  Larger products return
- * GEMM_ERR_SCRATCH_LIMIT and enqueue nothing.
+ * Limit: the scratch gemm() would take for the product -- 4 * M * roundup(K, 4)
+ * bytes for a re-strided A, 4 * K * roundup(N, 4) for a re-strided B, and
+ * 256 KB per split piece of the K split, each rounded up to 256 bytes -- must
+ * not exceed GEMM_NOALLOC_SCRATCH_BYTES (64 MiB).  Aligned products with
+ * K, N multiples of 4 need at most the split workspace (14.7 MB at 4096^3,
+ * 18.5 MB at 256 x 65536 x 256).  A product that needs more returns
+ * GEMM_ERR_SCRATCH_LIMIT and enqueues nothing.
  *
- * Set-up: the first call on a device (that device current) loads the buffer
- * and looks up its device address; make that first call before any stream
- * capture.  Every device that has made a call holds the buffer until the
- * process exits.
+ * Set-up and memory: the first call on a device (that device current) does
+ * the library's per-device set-up and looks up the buffer's device address,
+ * which loads this part of the library's device code, the 64 MiB buffer
+ * with it, onto the device.  Make that first call before the application
+ * reserves the rest of the device memory for itself, and before any stream
+ * capture; later calls allocate nothing.  With CUDA's lazy module loading
+ * (the default) only devices on which this entry point has been called hold
+ * the buffer; with CUDA_MODULE_LOADING=EAGER every device on which the
+ * process uses this library holds it.  It stays until the process exits.
  *
  * Sharing: every call on a device uses the same buffer, which keeps the last
  * call's contents (nothing in it needs to start at zero: every byte a call
- * reads was written by that call).  Calls whose kernels overlap on the GPU --
- * on different streams, or from different threads -- race on the buffer and
- * give wrong results: order them on one stream, or synchronise between them.
+ * reads was written earlier in that call).  Calls whose kernels overlap on
+ * the GPU -- on different streams, or from different threads -- race on the
+ * buffer and give wrong results: order them on one stream, or synchronise
+ * between them.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (64ll * 1024 * 1024)
 

@@ -7,8 +7,8 @@ CPU: both variants build and say which they are.  GPU: a child process loads
 the debug build and runs products along every kernel path -- FFMA interior
 and edge tiles, the in-kernel split of a partial last wave and the workspace
 split, the tensor kernels whole, with the last round split and all split,
-the 1-SM fallback, the small-product FFMA kernel, the re-stride, transpose
-and conversion passes, the alpha / beta update and K = 0 -- each checked
+the 1-SM fallback, the small-product FFMA kernel, the re-stride and
+conversion passes, the alpha / beta update and K = 0 -- each checked
 against the oracle, with no bounds report after any of them."""
 import ctypes
 import os
@@ -86,7 +86,8 @@ else:
         check("fp32", *shp)
     check("fp32", 2816, 256, 2816, sampled=True)
     check("fp32", 1000, 777, 1500, alpha=0.5, beta=-1.25)
-    # tensor kernels: re-strided K, scalar transpose / stores (N % 4 != 0),
+    # tensor kernels: re-strided A (K % 4 != 0), re-strided B and scalar
+    # stores (N % 4 != 0),
     # all tiles split (one pair tile, long K), the last round split
     for mode in tc_modes:
         for shp in [(1000, 777, 1500), (300, 700, 201), (256, 8192, 256)]:

@@ -44,15 +44,22 @@ def test_launch_count_counts_kernels(libgemm):
     # 256^3 is a small product: one launch of the 32 x 32-tile FFMA kernel
     libgemm.gemm(a, b, c, mode=libgemm.FP32)
     assert libgemm.launch_count() - n0 == 1
-    libgemm.gemm(a, b, c, mode=libgemm.TF32)                 # transpose of B + MMA kernel
-    assert libgemm.launch_count() - n0 == 3
-    # a K that is not a multiple of 4 floats makes the tensor path re-stride A too
+    libgemm.gemm(a, b, c, mode=libgemm.TF32)                 # the MMA kernel alone (B read as stored)
+    assert libgemm.launch_count() - n0 == 2
+    # a K that is not a multiple of 4 floats makes the tensor path re-stride A first
     a2 = torch.from_numpy(np.ascontiguousarray(A[:, :255])).cuda()
     b2 = torch.from_numpy(np.ascontiguousarray(B[:255])).cuda()
     n1 = libgemm.launch_count()
     libgemm.gemm(a2, b2, c, mode=libgemm.TF32)
     torch.cuda.synchronize()
-    assert libgemm.launch_count() - n1 == 3
+    assert libgemm.launch_count() - n1 == 2
+    # an N that is not a multiple of 4 floats re-strides B as well
+    b3 = torch.from_numpy(np.ascontiguousarray(B[:255, :254])).cuda()
+    c3 = torch.empty((256, 254), device="cuda")
+    n3 = libgemm.launch_count()
+    libgemm.gemm(a2, b3, c3, mode=libgemm.TF32)
+    torch.cuda.synchronize()
+    assert libgemm.launch_count() - n3 == 3
     # FP32_VIA_BF16: one conversion kernel for both operands + MMA kernel when
     # their rows are whole 16-byte chunks; two conversion kernels otherwise
     n2 = libgemm.launch_count()

@@ -4,7 +4,7 @@ mode gives the same C, bit for bit, as the same call made eagerly.
 The library's per-device set-up happens at the first call on a device, so
 each test makes one eager call before capturing.  Captured shapes include
 ones that take scratch from the library's stream-ordered pool inside the
-capture (the B^T pass of TF32, the BF16 rounding pass, the K-split
+capture (the re-strided A of K = 777, the BF16 rounding pass, the K-split
 workspaces) and so become graph memory nodes.
 """
 import numpy as np
