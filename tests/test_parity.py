@@ -130,16 +130,29 @@ def test_fp32_fma_chain_hand_cases(libgemm):
         assert float(C[0, 0]) == float(case["C"][0]), case["name"]
 
 
-@pytest.mark.parametrize("M,K,N", [(1000, 777, 1500), (4096, 4096, 4096), (129, 65, 257), (1, 1, 1),
-                                   (640, 96, 1028), (3, 4, 4)])
+# the one-launch conversion (rows of whole 16-byte chunks) and the
+# element-wise one, with whole tiles, the last round split (4096^3), all
+# tiles split (256 x 16384 x 256), partial tiles and long K
+VIA_BF16_SHAPES = [(1000, 777, 1500), (4096, 4096, 4096), (129, 65, 257), (1, 1, 1),
+                   (640, 96, 1028), (3, 4, 4), (256, 16384, 256), (3000, 2000, 1000),
+                   (8192, 512, 256), (256, 512, 8192), (2048, 8192, 2048), (1000, 4100, 1500)]
+
+
+@pytest.mark.parametrize("M,K,N", VIA_BF16_SHAPES)
 def test_fp32_via_bf16_equals_bf16_on_rounded_operands(libgemm, M, K, N):
     """GEMM_FP32_VIA_BF16 rounds float operands to bfloat16 on the GPU (to
     nearest, ties to even) and multiplies as GEMM_BF16: bit for bit the same
     as GEMM_BF16 on operands rounded on the host, and within the BF16
-    tolerance of the oracle on the original floats."""
+    tolerance of the oracle on the original floats (sampled entries above
+    2^31 multiply-adds)."""
     A, B = inputs.matrices(M, K, N, "pm1", seed=M + K + N)
     C = run(libgemm, A, B, "fp32_via_bf16")
     np.testing.assert_array_equal(C, run(libgemm, A, B, "bf16"))
     if M * N * K <= 2 ** 31:
         Cref, S = oracle.gemm(A, B)
         assert_within(C, Cref, S, TOL["fp32_via_bf16"], "fp32 via bf16")
+    else:
+        rows, cols = inputs.sample_indices(M, N, 4096)
+        Cref, S = oracle.dot(A, B, rows, cols)
+        assert_within(C[rows, cols], Cref, S, TOL["fp32_via_bf16"], "fp32 via bf16 sampled")
+
