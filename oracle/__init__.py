@@ -16,7 +16,9 @@ Input formats (``fmt``):
   "tf32"  float32 with the low 13 fraction bits cleared, then widened
           (a diagnostic for the TF32 tensor path);
   "f64"   float64 values as given;
-  "f16"   uint16 IEEE binary16 bit patterns, widened exactly.
+  "f16"   uint16 IEEE binary16 bit patterns, widened exactly;
+  "tf32rna"  float32 rounded to the nearest TF32 value (10 fraction bits),
+          ties away from zero, then widened.
 """
 from __future__ import annotations
 
@@ -32,9 +34,9 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 
-_FMT = {"f32": 0, "bf16": 1, "tf32": 2, "f64": 3, "f16": 4}
+_FMT = {"f32": 0, "bf16": 1, "tf32": 2, "f64": 3, "f16": 4, "tf32rna": 5}
 _DTYPE = {"f32": np.float32, "bf16": np.uint16, "tf32": np.float32, "f64": np.float64,
-          "f16": np.uint16}
+          "f16": np.uint16, "tf32rna": np.float32}
 
 _lock = threading.Lock()
 _lib = None

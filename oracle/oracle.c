@@ -34,6 +34,9 @@
  *     and clears the other 13 (truncation), then widens exactly.  FP16 values
  *     arrive as IEEE binary16 patterns (sign, 5 exponent bits with bias 15,
  *     10 fraction bits; exponent 0 holds the subnormals) and widen exactly.
+ *     The TF32-nearest format rounds a binary32 to the nearest value with 10
+ *     fraction bits, ties away from zero (the rounding of the GEMM_TF32_RN
+ *     mode), and widens that exactly.
  *
  * Each product of two widened binary32 values has at most 48 significant
  * bits and is therefore exact in double; only the running sums round.  The
@@ -71,7 +74,8 @@ enum {
     ORACLE_BF16 = 1,      /* bfloat16 bit patterns (uint16)           */
     ORACLE_TF32_TRUNC = 2,/* binary32, low 13 fraction bits cleared   */
     ORACLE_F64 = 3,       /* binary64 values, used as given           */
-    ORACLE_F16 = 4        /* IEEE binary16 bit patterns (uint16)      */
+    ORACLE_F16 = 4,       /* IEEE binary16 bit patterns (uint16)      */
+    ORACLE_TF32_RNA = 5   /* binary32 rounded to TF32, nearest, ties away */
 };
 
 static double from_bits32(uint32_t u) {
@@ -88,6 +92,27 @@ static double from_half(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* A binary32 value rounded to the nearest TF32 value, ties away from zero.
+ * TF32 keeps binary32's sign and 8-bit exponent and 10 fraction bits, so a
+ * value of magnitude in [2^e, 2^(e+1)) lies on a grid of spacing 2^(e-10)
+ * (for e >= -126; below, the subnormals, the spacing stays 2^-136).  The
+ * magnitude is split into the grid point below it and the remainder; a
+ * remainder of half the spacing or more rounds up (a tie goes away from
+ * zero).  Rounding up past the largest TF32 value, (2 - 2^-10) * 2^127, gives
+ * infinity.  Zero, infinity and NaN are kept.  Every step is exact in double. */
+static double tf32_nearest_away(float f) {
+    if (f == 0.0f || isinf(f) || isnan(f)) return (double)f;
+    const double a = fabs((double)f);
+    int e2 = 0;
+    (void)frexp(a, &e2);                /* a = m * 2^e2, m in [0.5, 1): a in [2^(e2-1), 2^e2) */
+    const int e = e2 - 1 < -126 ? -126 : e2 - 1;
+    const double spacing = ldexp(1.0, e - 10);
+    const double below = floor(a / spacing) * spacing;
+    double v = (a - below >= 0.5 * spacing) ? below + spacing : below;
+    if (v >= ldexp(1.0, 128)) v = INFINITY;
+    return f < 0.0f ? -v : v;
+}
+
 /* Element idx of an input matrix in format fmt, widened exactly to double. */
 static double widen(int fmt, const void* p, int64_t idx) {
     switch (fmt) {
@@ -102,6 +127,8 @@ static double widen(int fmt, const void* p, int64_t idx) {
     }
     case ORACLE_F16:
         return from_half(((const uint16_t*)p)[idx]);
+    case ORACLE_TF32_RNA:
+        return tf32_nearest_away(((const float*)p)[idx]);
     default:
         return ((const double*)p)[idx];
     }
@@ -109,7 +136,7 @@ static double widen(int fmt, const void* p, int64_t idx) {
 
 static int valid(int fmt, const void* A, const void* B, int64_t M, int64_t K,
                  int64_t N) {
-    if (fmt < ORACLE_F32 || fmt > ORACLE_F16) return 0;
+    if (fmt < ORACLE_F32 || fmt > ORACLE_TF32_RNA) return 0;
     if (M < 0 || K < 0 || N < 0) return 0;
     if ((M > 0 && K > 0 && !A) || (K > 0 && N > 0 && !B)) return 0;
     return 1;
@@ -304,7 +331,7 @@ int oracle_update_f32(const float* P, const float* C_in, int64_t n, float alpha,
 
 /* Element-wise widening of n inputs of format fmt (to test the formats). */
 int oracle_widen(int fmt, const void* p, int64_t n, double* out) {
-    if (fmt < ORACLE_F32 || fmt > ORACLE_F16 || n < 0 || (n > 0 && (!p || !out)))
+    if (fmt < ORACLE_F32 || fmt > ORACLE_TF32_RNA || n < 0 || (n > 0 && (!p || !out)))
         return -1;
     for (int64_t t = 0; t < n; ++t) out[t] = widen(fmt, p, t);
     return 0;

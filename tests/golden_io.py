@@ -77,3 +77,16 @@ def update_hand():
         assert c["A"].shape == (m, k) and c["B"].shape == (k, n)
         assert c["C_in"].shape == (m, n) and c["OUT"].shape == (m, n)
     return cases
+
+
+def tf32_rna():
+    """Parse tf32_rna.txt: a list of (input pattern, rounded pattern) as uint32."""
+    rows = []
+    with open(os.path.join(GOLDEN, "tf32_rna.txt")) as f:
+        for raw in f:
+            line = raw.split("#")[0].strip()
+            if not line:
+                continue
+            a, b = line.split()
+            rows.append((int(a, 16), int(b, 16)))
+    return rows

@@ -204,11 +204,48 @@ def test_tf32_truncation_known_values():
     assert list(oracle.widen(x, "f32")) == [float(v) for v in x]
 
 
+def test_tf32_rna_hand_worked_patterns():
+    """tests/golden/tf32_rna.txt: ties, carries into the exponent, subnormals,
+    overflow to infinity, signed zeros."""
+    from golden_io import tf32_rna
+    rows = tf32_rna()
+    x = np.array([a for a, _ in rows], np.uint32).view(np.float32)
+    want = np.array([b for _, b in rows], np.uint32).view(np.float32).astype(np.float64)
+    got = oracle.widen(x, "tf32rna")
+    np.testing.assert_array_equal(got, want)
+    assert list(np.signbit(got)) == list(np.signbit(want))
+
+
+def test_tf32_rna_is_the_nearest_tf32_value():
+    """For many finite binary32 values: the result is a TF32 value (no bits
+    below the top 10 fraction bits), no TF32 value is nearer -- the two
+    candidates are the value with the 13 low bits cleared and the next one
+    up in magnitude -- and of two equally near ones the larger magnitude is
+    taken."""
+    rng = np.random.default_rng(7)
+    u = rng.integers(0, 0x7F7FF000, size=200000, dtype=np.uint64).astype(np.uint32)
+    u = np.concatenate([u, (u & np.uint32(0xFFFFE000)) | np.uint32(0x1000)])   # ties
+    u = np.concatenate([u, u | np.uint32(0x80000000)])                          # negatives
+    x = u.view(np.float32)
+    got = oracle.widen(x, "tf32rna")
+    assert np.all(np.isfinite(got))
+    g32 = got.astype(np.float32)
+    assert np.array_equal(g32.astype(np.float64), got)            # exact in binary32
+    assert not np.any(g32.view(np.uint32) & np.uint32(0x1FFF))    # and a TF32 value
+    down = (u & np.uint32(0xFFFFE000)).view(np.float32).astype(np.float64)
+    up = ((u & np.uint32(0xFFFFE000)) + np.uint32(0x2000)).view(np.float32).astype(np.float64)
+    xd = x.astype(np.float64)
+    dd, du = np.abs(xd - down), np.abs(up - xd)
+    want = np.where(du <= dd, up, down)
+    np.testing.assert_array_equal(got, want)
+
+
 def test_formats_agree_on_exact_inputs():
     # integers -4..4 are exact in every format, so every format gives one C
     A, B = inputs.matrices(9, 31, 11, "int4", seed=12)
     ref, _ = oracle.gemm(A, B, fmt="f32")
-    for fmt, (a, b) in {"tf32": (A, B), "bf16": (inputs.bf16_bits(A), inputs.bf16_bits(B)),
+    for fmt, (a, b) in {"tf32": (A, B), "tf32rna": (A, B),
+                        "bf16": (inputs.bf16_bits(A), inputs.bf16_bits(B)),
                         "f16": (inputs.fp16_bits(A), inputs.fp16_bits(B)),
                         "f64": (A.astype(np.float64), B.astype(np.float64))}.items():
         C, _ = oracle.gemm(a, b, fmt=fmt)
