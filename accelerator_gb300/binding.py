@@ -12,8 +12,9 @@ import threading
 
 from . import build as _build
 
-FP32, TF32, BF16, FP16, FP32_VIA_BF16 = 0, 1, 2, 3, 4
-MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16, "fp16": FP16, "fp32_via_bf16": FP32_VIA_BF16}
+FP32, TF32, BF16, FP16, FP32_VIA_BF16, TF32_RN = 0, 1, 2, 3, 4, 5
+MODES = {"fp32": FP32, "tf32": TF32, "bf16": BF16, "fp16": FP16, "fp32_via_bf16": FP32_VIA_BF16,
+         "tf32_rn": TF32_RN}
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -144,7 +145,7 @@ def _operands(A, B, C, mode):
         mode = MODES[mode.lower()]
     if not _WANT:
         _WANT.update({FP32: torch.float32, TF32: torch.float32, BF16: torch.bfloat16,
-                      FP16: torch.float16, FP32_VIA_BF16: torch.float32})
+                      FP16: torch.float16, FP32_VIA_BF16: torch.float32, TF32_RN: torch.float32})
     want = _WANT.get(mode, torch.float32)
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shapes {tuple(A.shape)} and {tuple(B.shape)} do not chain")

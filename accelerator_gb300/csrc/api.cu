@@ -281,6 +281,37 @@ int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64
     return rc;
 }
 
+// GEMM_TF32_RN: round A and B to TF32 to nearest (ties away from zero) into
+// scratch rows whose stride is a multiple of 16 bytes, then the TF32 product
+// (which reads these rounded values exactly; the split workspace, when the
+// product is split, after them).
+int rounded_tf32_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
+                      const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
+    const int64_t lda = round_up(K, 4), ldb = round_up(N, 4);
+    const int64_t a_bytes = round_up(M * lda * 4, 256), b_bytes = round_up(K * ldb * 4, 256);
+    const TcSplit split = tc_plan_split(TcMode::kTF32, M, N, K);
+    const int64_t ws_bytes = round_up(tc_split_workspace_bytes(split, M, N), 256);
+    void* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, (size_t)(a_bytes + b_bytes + ws_bytes), st->pool,
+                                stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_MEMORY;
+    }
+    uint8_t* s = static_cast<uint8_t*>(scratch);
+    float* a_r = reinterpret_cast<float*>(s);
+    float* b_r = reinterpret_cast<float*>(s + a_bytes);
+    int rc = GEMM_OK, launched = 0;
+    if (launch_to_tf32_pair(A, a_r, M, K, lda, B, b_r, K, N, ldb, stream, &launched) !=
+        cudaSuccess)
+        rc = GEMM_ERR_CUDA;
+    g_launches += launched;
+    if (rc == GEMM_OK)
+        rc = tc_launch(TcMode::kTF32, a_r, lda, b_r, ldb, C, M, K, N, epi, split,
+                       ws_bytes ? s + a_bytes + b_bytes : nullptr, st, stream);
+    if (cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
+    return rc;
+}
+
 }  // namespace
 
 // Internal hooks for other translation units of this library (declared in
@@ -351,7 +382,8 @@ namespace {
 int gemm_impl(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
               float alpha, float beta, int precision_mode, cudaStream_t stream) {
     if (precision_mode != GEMM_FP32 && precision_mode != GEMM_TF32 && precision_mode != GEMM_BF16 &&
-        precision_mode != GEMM_FP16 && precision_mode != GEMM_FP32_VIA_BF16)
+        precision_mode != GEMM_FP16 && precision_mode != GEMM_FP32_VIA_BF16 &&
+        precision_mode != GEMM_TF32_RN)
         return GEMM_ERR_INVALID_ARG;
     if (M < 0 || K < 0 || N < 0) return GEMM_ERR_INVALID_ARG;
     // Every dimension must fit the kernels' 32-bit indices and TMA coordinates.
@@ -391,6 +423,9 @@ int gemm_impl(const void* A, const void* B, float* C, int64_t M, int64_t K, int6
                                                       st, stream);
     if (precision_mode == GEMM_FP32_VIA_BF16)
         return rounded_bf16_gemm(static_cast<const float*>(A), static_cast<const float*>(B), C, M,
+                                 K, N, epi, st, stream);
+    if (precision_mode == GEMM_TF32_RN)
+        return rounded_tf32_gemm(static_cast<const float*>(A), static_cast<const float*>(B), C, M,
                                  K, N, epi, st, stream);
     const TcMode tm = precision_mode == GEMM_BF16   ? TcMode::kBF16
                       : precision_mode == GEMM_FP16 ? TcMode::kF16
@@ -451,7 +486,7 @@ int gemm_debug_status(struct CUstream_st* stream_) {
 
 int gemm_debug_build(void) { return kDebugBuild ? 1 : 0; }
 
-int gemm_version(void) { return 100; }
+int gemm_version(void) { return 200; }
 
 int64_t gemm_launch_count(void) { return g_launches.load(); }
 

@@ -154,6 +154,13 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t rows, int64_t co
 cudaError_t launch_to_bf16_pair(const float* a, void* a_dst, int64_t a_rows, int64_t a_cols,
                                 int64_t a_ld, const float* b, void* b_dst, int64_t b_rows,
                                 int64_t b_cols, int64_t b_ld, cudaStream_t stream, int* launches);
+// GEMM_TF32_RN: both operands rounded to TF32 (to nearest, ties away from
+// zero; binary32 with the 13 low fraction bits zero) into rows of stride
+// a_ld / b_ld floats, one launch when both operands' rows allow 16-byte
+// loads and stores, else one element-wise launch each.
+cudaError_t launch_to_tf32_pair(const float* a, float* a_dst, int64_t a_rows, int64_t a_cols,
+                                int64_t a_ld, const float* b, float* b_dst, int64_t b_rows,
+                                int64_t b_cols, int64_t b_ld, cudaStream_t stream, int* launches);
 cudaError_t launch_fill_zero(float* C, int64_t n, cudaStream_t stream);
 // C := beta * C over n elements, each rounded once (beta != 0).
 cudaError_t launch_scale(float* C, int64_t n, float beta, cudaStream_t stream);

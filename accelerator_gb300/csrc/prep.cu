@@ -3,6 +3,8 @@
 //   restride    copies an operand into a buffer whose row stride is a multiple
 //               of 16 bytes, for the tensor-core path when TMA cannot describe
 //               the caller's layout (e.g. K = 777 floats: 3108-byte rows).
+//   to_bf16 / to_tf32  the rounding passes of GEMM_FP32_VIA_BF16 and
+//               GEMM_TF32_RN (to nearest; ties to even / away from zero).
 //   fill_zero   C := 0 for K == 0 (the empty sum).
 //   scale       C := beta * C, the generalised product when alpha == 0 or K == 0.
 //   splitk_reduce  adds the K-split partials of the tensor kernel in split
@@ -61,6 +63,64 @@ struct Bf16Job {
     uint2* dst;
     int64_t rows, cols4, dst_ld4;
 };
+
+// float -> TF32, round to nearest with ties away from zero (cvt.rna.tf32.f32),
+// kept as a binary32 whose 13 low fraction bits are zero.
+__device__ __forceinline__ float round_tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r & 0xFFFFE000u);
+}
+
+// The TF32 rounding pass of GEMM_TF32_RN: both operands in one launch, laid
+// out like the bfloat16 pass (one row per block and pass, four 16-byte
+// loads in flight per thread), writing rounded floats into rows of stride
+// dst_ld4 float4s.
+struct Tf32Job {
+    const float4* src;
+    float4* dst;
+    int64_t rows, cols4, dst_ld4;
+};
+
+__global__ void __launch_bounds__(256) to_tf32_pair_kernel(Tf32Job a, Tf32Job b) {
+    grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
+    const int64_t total = a.rows + b.rows;
+    for (int64_t rr = blockIdx.x; rr < total; rr += gridDim.x) {
+        const bool in_a = rr < a.rows;
+        const Tf32Job& j = in_a ? a : b;
+        const int64_t r = in_a ? rr : rr - a.rows;
+        const float4* s = j.src + r * j.cols4;
+        float4* d = j.dst + r * j.dst_ld4;
+        for (int64_t c0 = threadIdx.x; c0 < j.cols4; c0 += 4 * (int64_t)blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t c = c0 + q * (int64_t)blockDim.x;
+                v[q] = c < j.cols4 && GEMM_DBG_OK(s + c, j.src, j.rows * j.cols4 * 16, 16)
+                           ? __ldcs(s + c)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t c = c0 + q * (int64_t)blockDim.x;
+                if (c < j.cols4 && GEMM_DBG_OK(d + c, j.dst, j.rows * j.dst_ld4 * 16, 16))
+                    d[c] = make_float4(round_tf32_rna(v[q].x), round_tf32_rna(v[q].y),
+                                       round_tf32_rna(v[q].z), round_tf32_rna(v[q].w));
+            }
+        }
+    }
+}
+
+// Element-wise form for rows that are not whole 16-byte chunks.
+__global__ void to_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                               int64_t rows, int64_t cols, int64_t dst_ld) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x)
+            if (GEMM_DBG_OK(src + r * cols + c, src, rows * cols * 4, 4) &&
+                GEMM_DBG_OK(dst + r * dst_ld + c, dst, rows * dst_ld * 4, 4))
+                dst[r * dst_ld + c] = round_tf32_rna(src[r * cols + c]);
+}
 
 __global__ void __launch_bounds__(256) to_bf16_pair_kernel(Bf16Job a, Bf16Job b) {
     grid_launch_dependents();   // the MMA kernel may start its set-up meanwhile
@@ -254,6 +314,41 @@ cudaError_t launch_to_bf16_pair(const float* a, void* a_dst, int64_t a_rows, int
     const int64_t rows = a_rows + b_rows;
     const unsigned grid = (unsigned)(rows < (1 << 20) ? rows : (1 << 20));
     to_bf16_pair_kernel<<<grid, 256, 0, stream>>>(ja, jb);
+    *launches = 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_tf32_pair(const float* a, float* a_dst, int64_t a_rows, int64_t a_cols,
+                                int64_t a_ld, const float* b, float* b_dst, int64_t b_rows,
+                                int64_t b_cols, int64_t b_ld, cudaStream_t stream, int* launches) {
+    auto vec_ok = [](const float* src, const float* dst, int64_t cols, int64_t ld) {
+        return cols % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+               (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+    };
+    *launches = 0;
+    if (a_rows <= 0 || a_cols <= 0 || b_rows <= 0 || b_cols <= 0 ||
+        !vec_ok(a, a_dst, a_cols, a_ld) || !vec_ok(b, b_dst, b_cols, b_ld)) {
+        const float* src[2] = {a, b};
+        float* dst[2] = {a_dst, b_dst};
+        const int64_t rows[2] = {a_rows, b_rows}, cols[2] = {a_cols, b_cols}, ld[2] = {a_ld, b_ld};
+        for (int t = 0; t < 2; ++t) {
+            if (rows[t] <= 0 || cols[t] <= 0) continue;
+            const int64_t bx = (cols[t] + 255) / 256;
+            dim3 grid((unsigned)(bx < 64 ? bx : 64), (unsigned)(rows[t] < 65535 ? rows[t] : 65535));
+            to_tf32_kernel<<<grid, 256, 0, stream>>>(src[t], dst[t], rows[t], cols[t], ld[t]);
+            ++*launches;
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    const Tf32Job ja{reinterpret_cast<const float4*>(a), reinterpret_cast<float4*>(a_dst), a_rows,
+                     a_cols / 4, a_ld / 4};
+    const Tf32Job jb{reinterpret_cast<const float4*>(b), reinterpret_cast<float4*>(b_dst), b_rows,
+                     b_cols / 4, b_ld / 4};
+    const int64_t rows = a_rows + b_rows;
+    const unsigned grid = (unsigned)(rows < (1 << 20) ? rows : (1 << 20));
+    to_tf32_pair_kernel<<<grid, 256, 0, stream>>>(ja, jb);
     *launches = 1;
     return cudaGetLastError();
 }

@@ -108,6 +108,17 @@ def fp16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
+def tf32_rna(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to TF32 (10 fraction bits) to nearest, ties away
+    from zero: half a TF32 unit (bit 12) added to the pattern, then the 13 low
+    bits cleared (a carry moves into the exponent).  Finite inputs only.  The
+    input recipe for feeding GEMM_TF32 operands rounded the way GEMM_TF32_RN
+    rounds them."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + np.uint64(0x1000)) & np.uint64(0xFFFFE000)).astype(np.uint32)
+    return r.view(np.float32)
+
+
 def tf32_exact(x: np.ndarray) -> np.ndarray:
     """float32 values with the low 13 fraction bits cleared, so every value is
     exactly representable in TF32 and the tensor cores read it unchanged."""

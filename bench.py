@@ -44,9 +44,10 @@ METRIC = "GEMM TFLOP/s (FP32 and TF32/BF16) at N=4096, % of sm_103a peak"
 UNIT = "TFLOP/s"
 MODES = ("fp32", "tf32", "bf16")               # the bench line's step
 # further modes that --modes can select, to time or profile their kernels:
-# binary16 inputs (the BF16 kernel's kind::f16 with f16 operands) and FP32
-# data rounded to bfloat16 by a conversion launch before the BF16 kernel
-EXTRA_MODES = ("fp16", "fp32_via_bf16")
+# binary16 inputs (the BF16 kernel's kind::f16 with f16 operands), FP32
+# data rounded to bfloat16 by a conversion launch before the BF16 kernel,
+# and FP32 data rounded to TF32 to nearest by a launch before the TF32 kernel
+EXTRA_MODES = ("fp16", "fp32_via_bf16", "tf32_rn")
 ALL_MODES = MODES + EXTRA_MODES
 L2_FLUSH_BYTES = 256 << 20
 
@@ -58,7 +59,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 TF32_PER_BF16 = 1.1 / 2.25                   # nominal dense TF32 / BF16 tensor rates
 NOMINAL_TFLOPS = {"bf16": 2250.0, "tf32": 1100.0, "fp16": 2250.0,
-                  "fp32_via_bf16": 2250.0}   # stated dense peaks (no sparsity)
+                  "fp32_via_bf16": 2250.0, "tf32_rn": 1100.0}   # stated dense peaks (no sparsity)
 
 # DRAM traffic of one launch of the dominant kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
@@ -324,7 +325,8 @@ def run_libgemm(args):
     a16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16).to(dev)
     b16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16).to(dev)
     ops = {"fp32": (a32, b32, binding.FP32), "tf32": (a32, b32, binding.TF32),
-           "bf16": (a16, b16, binding.BF16), "fp32_via_bf16": (a32, b32, binding.FP32_VIA_BF16)}
+           "bf16": (a16, b16, binding.BF16), "fp32_via_bf16": (a32, b32, binding.FP32_VIA_BF16),
+           "tf32_rn": (a32, b32, binding.TF32_RN)}
     if "fp16" in args.modes:
         ops["fp16"] = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).view(torch.float16).to(dev),
                        torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).view(torch.float16).to(dev),
@@ -403,6 +405,9 @@ def run_libgemm(args):
             peak, bound, note = tf32_peak, "tensor", f"{src} bf16 x nominal tf32/bf16 ratio"
         elif m == "fp32_via_bf16":
             peak, bound, note = bf16_peak, "tensor", f"{src} bf16 burst (conversion launch included in the time)"
+        elif m == "tf32_rn":
+            peak, bound, note = tf32_peak, "tensor", (f"{src} bf16 x nominal tf32/bf16 ratio "
+                                                      "(rounding launch included in the time)")
         else:   # bf16, fp16: one kind::f16 rate
             peak, bound, note = bf16_peak, "tensor", f"{src} bf16 burst"
         modes_out[m] = {"ms_mean": ms, "ms_median": float(np.median(per_mode[m])),
@@ -451,8 +456,8 @@ def run_libgemm(args):
 # The input set each mode reads on the end-to-end leg: A and B as float32
 # serve FP32, TF32 and FP32_VIA_BF16; bfloat16 and binary16 copies serve the
 # others.  Bytes per element of each set.
-E2E_GROUP_OF = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "bf16": "bf16",
-                "fp16": "fp16"}
+E2E_GROUP_OF = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "tf32_rn": "f32",
+                "bf16": "bf16", "fp16": "fp16"}
 E2E_GROUP_BYTES = {"f32": 4, "bf16": 2, "fp16": 2}
 
 
@@ -480,7 +485,8 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     import torch
     from accelerator_gb300 import binding, inputs
     mode_ids = {"fp32": binding.FP32, "tf32": binding.TF32, "bf16": binding.BF16,
-                "fp16": binding.FP16, "fp32_via_bf16": binding.FP32_VIA_BF16}
+                "fp16": binding.FP16, "fp32_via_bf16": binding.FP32_VIA_BF16,
+                "tf32_rn": binding.TF32_RN}
     group_of = E2E_GROUP_OF
     host = {}
     for g in e2e_input_groups(args.modes):

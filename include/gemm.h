@@ -70,7 +70,14 @@ enum gemm_mode {
      * ties to even) in a conversion pass, then multiplies as GEMM_BF16:
      * BF16 tensor-core speed for float data, at BF16 input precision.  The
      * result equals GEMM_BF16 on the caller-rounded operands, bit for bit. */
-    GEMM_FP32_VIA_BF16 = 4
+    GEMM_FP32_VIA_BF16 = 4,
+    /* A, B: const float*.  As GEMM_TF32, but the library first rounds each
+     * input to the nearest TF32 value (ties away from zero) in a conversion
+     * pass, instead of letting the tensor cores drop the 13 low fraction
+     * bits: the rounding errors of the inputs then have no sign bias, at the
+     * cost of the pass (scratch for the rounded copies of A and B).  The
+     * result equals GEMM_TF32 on the caller-rounded operands, bit for bit. */
+    GEMM_TF32_RN = 5
 };
 
 /* Status codes returned by every entry point (0 = success). */
@@ -104,8 +111,8 @@ enum gemm_status {
  *                   K == 0: C is set to 0 (the empty sum).
  *   precision_mode  one of enum gemm_mode
  *   stream          stream to enqueue on
- * GEMM_FP32_VIA_BF16 takes scratch for the rounded copies of A and B, from the
- * same stream-ordered allocator.
+ * GEMM_FP32_VIA_BF16 and GEMM_TF32_RN take scratch for the rounded copies of A
+ * and B, from the same stream-ordered allocator.
  * Any alignment of element size or more is accepted.  When a tensor-core mode
  * meets a row stride that is not a multiple of 16 bytes, or a base address
  * that is not 16-byte aligned, the operand is first copied into a scratch

@@ -9,7 +9,8 @@ from __future__ import annotations
 
 import numpy as np
 
-TOL = {"fp32": 1e-5, "tf32": 2e-3, "bf16": 1e-2, "fp16": 2e-3, "fp32_via_bf16": 1e-2}
+TOL = {"fp32": 1e-5, "tf32": 2e-3, "bf16": 1e-2, "fp16": 2e-3, "fp32_via_bf16": 1e-2,
+       "tf32_rn": 2e-3}
 
 # Diagnostic tolerances when the oracle sees the same rounded inputs as the
 # tensor cores (TF32-truncated or BF16 values): only the binary32

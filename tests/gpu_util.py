@@ -40,4 +40,6 @@ def oracle_inputs(A: np.ndarray, B: np.ndarray, mode: str):
         return inputs.fp16_bits(A), inputs.fp16_bits(B), "f16"
     if mode == "tf32":
         return A, B, "tf32"
+    if mode == "tf32_rn":
+        return A, B, "tf32rna"
     return A, B, "f32"

@@ -34,11 +34,11 @@ def test_status_strings(libgemm):
         s = libgemm.status_string(code)
         assert s and s != "unknown status"
     assert libgemm.status_string(99) == "unknown status"
-    assert libgemm.version() == 100
+    assert libgemm.version() == 200
     assert libgemm.launch_count() >= 0
 
 
-@pytest.mark.parametrize("mode", [-1, 5, 17])
+@pytest.mark.parametrize("mode", [-1, 6, 17])
 def test_bad_mode(libgemm, mode):
     assert libgemm.gemm_raw(FAKE, FAKE + 4096, FAKE + 8192, 4, 4, 4, mode) == libgemm.ERR_INVALID_ARG
 
@@ -95,7 +95,7 @@ def test_no_device_is_an_error_not_a_crash(libgemm):
 def test_gemm_ex_validates_like_gemm(libgemm):
     G = 1 << 20
     ex = libgemm.gemm_ex_raw
-    assert ex(FAKE, FAKE + G, FAKE + 2 * G, 4, 4, 4, 2.0, 1.0, 5) == libgemm.ERR_INVALID_ARG
+    assert ex(FAKE, FAKE + G, FAKE + 2 * G, 4, 4, 4, 2.0, 1.0, 6) == libgemm.ERR_INVALID_ARG
     assert ex(FAKE, FAKE, FAKE, -1, 4, 4, 2.0, 1.0, 0) == libgemm.ERR_INVALID_ARG
     assert ex(0, 0, 0, 0, 5, 5, 2.0, 1.0, 0) == libgemm.OK          # empty C: nothing to do
     assert ex(0, FAKE + G, FAKE + 2 * G, 4, 4, 4, 2.0, 1.0, 0) == libgemm.ERR_INVALID_ARG

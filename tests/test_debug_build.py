@@ -7,8 +7,8 @@ CPU: both variants build and say which they are.  GPU: a child process loads
 the debug build and runs products along every kernel path -- FFMA interior
 and edge tiles, the in-kernel split of a partial last wave and the workspace
 split, the tensor kernels whole, with the last round split and all split,
-the 1-SM fallback, the small-product FFMA kernel, the re-stride and
-conversion passes, the alpha / beta update and K = 0 -- each checked
+the 1-SM fallback, the small-product FFMA kernel, the re-stride and the
+bfloat16 and TF32 rounding passes, the alpha / beta update and K = 0 -- each checked
 against the oracle, with no bounds report after any of them."""
 import ctypes
 import os
@@ -94,9 +94,11 @@ else:
             check(mode, *shp)
         check(mode, 4096, 4096, 4096, sampled=True)
         check(mode, 1000, 777, 1500, alpha=2.0, beta=0.75)
-    # conversion pass: vector and element-wise forms
+    # conversion passes: vector and element-wise forms
     check("fp32_via_bf16", 640, 96, 1028)
     check("fp32_via_bf16", 300, 700, 201)
+    check("tf32_rn", 640, 96, 1028)
+    check("tf32_rn", 300, 700, 201)
     # K = 0: fill and scale
     for mode in ("fp32", "bf16"):
         check(mode, 64, 0, 96)
@@ -118,7 +120,7 @@ def _child(env_extra):
 @pytest.mark.gpu
 def test_debug_build_all_paths_in_bounds():
     out = _child({})
-    assert out.count("ok ") == 28
+    assert out.count("ok ") == 30
 
 
 @pytest.mark.gpu

@@ -68,3 +68,10 @@ def test_launch_count_counts_kernels(libgemm):
     libgemm.gemm(a2, b2, c, mode=libgemm.FP32_VIA_BF16)
     torch.cuda.synchronize()
     assert libgemm.launch_count() - n2 == 5
+    # TF32_RN: the same shape of launches with the TF32 rounding pass
+    n4 = libgemm.launch_count()
+    libgemm.gemm(a, b, c, mode=libgemm.TF32_RN)
+    assert libgemm.launch_count() - n4 == 2
+    libgemm.gemm(a2, b2, c, mode=libgemm.TF32_RN)
+    torch.cuda.synchronize()
+    assert libgemm.launch_count() - n4 == 5

@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [("fp32", 1000, 777, 1500), ("tf32", 1000, 777, 1500), ("bf16", 1000, 777, 1500),
          ("fp16", 1000, 777, 1500), ("fp32_via_bf16", 1000, 777, 1500),
+         ("tf32_rn", 1000, 777, 1500),
          ("bf16", 256, 16384, 256), ("tf32", 4096, 512, 4096), ("fp32", 256, 4096, 256),
          ("fp32", 4096, 256, 4096)]
 
@@ -25,7 +26,7 @@ CASES = [("fp32", 1000, 777, 1500), ("tf32", 1000, 777, 1500), ("bf16", 1000, 77
 def test_capture_and_replay(libgemm, mode, M, K, N):
     import torch
     A, B = inputs.matrices(M, K, N, "pm1", seed=M + N)
-    a, b = device_operands(A, B, "fp32" if mode == "fp32_via_bf16" else mode)
+    a, b = device_operands(A, B, mode)
     m = libgemm.MODES[mode]
     eager = torch.empty((M, N), dtype=torch.float32, device="cuda")
     libgemm.gemm(a, b, eager, mode=m)

@@ -48,6 +48,18 @@ def test_bf16_round_to_nearest_even():
     assert abs(float(back[0]) / 3.0e38 - 1) < 2.0 ** -8
 
 
+def test_tf32_rna_recipe_matches_the_oracle_format():
+    """The host-side TF32 rounding recipe (a bit trick) and the oracle's
+    format (the grid definition) agree on finite values, ties included."""
+    import oracle
+    rng = np.random.default_rng(3)
+    u = rng.integers(0, 0x7F7FE000, size=100000, dtype=np.uint64).astype(np.uint32)
+    u = np.concatenate([u, (u & np.uint32(0xFFFFE000)) | np.uint32(0x1000)])
+    u = np.concatenate([u, u | np.uint32(0x80000000)])
+    x = u.view(np.float32).reshape(1, -1)
+    np.testing.assert_array_equal(inputs.tf32_rna(x).astype(np.float64), oracle.widen(x, "tf32rna"))
+
+
 def test_sample_indices_cover_edges():
     rows, cols = inputs.sample_indices(1000, 1500, n=4096)
     assert rows.dtype == np.int64 and rows.shape == cols.shape

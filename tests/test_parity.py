@@ -7,7 +7,8 @@ Workloads are the seeded synthetic inputs of the pages' studies:
   * the square sweep N = 128 .. 4096 (full oracle up to 1024, then 4096+
     sampled entries and the sum-of-all-elements identity);
   * 8192^3 on the tensor-core modes, uniform on [-1, 1).
-FP16 (binary16 inputs, the tolerance of TF32) rides along in every mode list.
+FP16 (binary16 inputs, the tolerance of TF32) and TF32_RN (inputs rounded to
+TF32 to nearest) ride along in every mode list.
 Every element must satisfy |C - Cref| <= tol * S_ij; C is poisoned with NaN
 before each launch so an unwritten element fails.
 """
@@ -21,7 +22,7 @@ from gpu_util import oracle_inputs, run
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["fp32", "tf32", "bf16", "fp16"]
+MODES = ["fp32", "tf32", "bf16", "fp16", "tf32_rn"]
 
 
 def _full_case(libgemm, oracle_cache, M, K, N, dist, mode):
@@ -75,7 +76,7 @@ def test_sweep_small_full(libgemm, oracle_cache, mode, n):
     _full_case(libgemm, oracle_cache, n, n, n, "u01", mode)
 
 
-@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16"])
+@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16", "tf32_rn"])
 def test_same_inputs_diagnostic(libgemm, mode):
     """Tensor path against the oracle fed the very values the tensor cores
     read (TF32-exact or BF16 values): only binary32 accumulation differs."""
@@ -104,7 +105,7 @@ def test_sweep_large_sampled(libgemm, mode, n):
     _sampled_case(libgemm, n, n, n, "u01", mode)
 
 
-@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16"])
+@pytest.mark.parametrize("mode", ["tf32", "bf16", "fp16", "tf32_rn"])
 def test_large_8192_sampled(libgemm, mode):
     _sampled_case(libgemm, 8192, 8192, 8192, "pm1", mode)
 
@@ -156,3 +157,27 @@ def test_fp32_via_bf16_equals_bf16_on_rounded_operands(libgemm, M, K, N):
         Cref, S = oracle.dot(A, B, rows, cols)
         assert_within(C[rows, cols], Cref, S, TOL["fp32_via_bf16"], "fp32 via bf16 sampled")
 
+
+
+@pytest.mark.parametrize("M,K,N", [(1000, 777, 1500), (4096, 4096, 4096), (256, 16384, 256),
+                                   (129, 65, 257), (640, 96, 1028)])
+def test_tf32_rn_equals_tf32_on_rounded_operands(libgemm, M, K, N):
+    """GEMM_TF32_RN rounds float operands to TF32 to nearest (ties away from
+    zero) on the GPU and multiplies as GEMM_TF32: bit for bit GEMM_TF32 on
+    operands rounded on the host the same way (one conversion launch for
+    aligned rows, element-wise launches otherwise)."""
+    A, B = inputs.matrices(M, K, N, "pm1", seed=M + 3 * K + N)
+    C = run(libgemm, A, B, "tf32_rn")
+    np.testing.assert_array_equal(C, run(libgemm, inputs.tf32_rna(A), inputs.tf32_rna(B), "tf32"))
+
+
+def test_tf32_rn_removes_the_truncation_bias(libgemm):
+    """On inputs uniform on [0, 1) every truncated operand is too small, so
+    GEMM_TF32's C sits below the exact product on average; rounding to
+    nearest has no such bias.  Mean signed error relative to S, full C."""
+    A, B = inputs.matrices(512, 2048, 512, "u01", seed=21)
+    Cref, S = oracle.gemm(A, B)
+    bias = {m: float(np.mean((run(libgemm, A, B, m).astype(np.float64) - Cref) / S))
+            for m in ("tf32", "tf32_rn")}
+    assert bias["tf32"] < -2e-4, bias            # about -2^-11 per operand, both operands
+    assert abs(bias["tf32_rn"]) < 0.1 * abs(bias["tf32"]), bias

@@ -14,7 +14,7 @@ from checks import TOL, assert_update_within
 
 pytestmark = pytest.mark.gpu
 
-MODES = ("fp32", "tf32", "bf16", "fp16", "fp32_via_bf16")
+MODES = ("fp32", "tf32", "bf16", "fp16", "fp32_via_bf16", "tf32_rn")
 
 
 def _cases(seed, n, p_big):
@@ -45,7 +45,8 @@ def _operands(A, B, mode):
     if mode == "fp32_via_bf16":   # the oracle sees the bfloat16 roundings
         return (torch.from_numpy(A), torch.from_numpy(B), inputs.bf16_bits(A),
                 inputs.bf16_bits(B), "bf16")
-    return torch.from_numpy(A), torch.from_numpy(B), A, B, ("tf32" if mode == "tf32" else "f32")
+    fmt = {"tf32": "tf32", "tf32_rn": "tf32rna"}.get(mode, "f32")
+    return torch.from_numpy(A), torch.from_numpy(B), A, B, fmt
 
 
 def _placed(host, offset, shape):

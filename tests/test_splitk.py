@@ -64,7 +64,7 @@ def test_fp32_wide_split(libgemm, M, K, N):
     _sampled(libgemm, M, K, N, "fp32")
 
 
-@pytest.mark.parametrize("mode", TC_MODES + ["fp32_via_bf16", "fp32"])
+@pytest.mark.parametrize("mode", TC_MODES + ["fp32_via_bf16", "tf32_rn", "fp32"])
 @pytest.mark.parametrize("M,K,N", [(300, 9001, 203), (257, 4100, 130), (100, 5000, 77)])
 def test_ragged_split_full(libgemm, mode, M, K, N):
     A, B = inputs.matrices(M, K, N, "pm1", seed=M * 3 + N)
@@ -77,7 +77,7 @@ def test_ragged_split_full(libgemm, mode, M, K, N):
     assert_within(C, Cref, S, TOL[mode], f"{mode} {M}x{K}x{N} (f32 inputs)")
 
 
-ALL_MODES = ["tf32", "bf16", "fp16", "fp32", "fp32_via_bf16"]
+ALL_MODES = ["tf32", "bf16", "fp16", "fp32", "fp32_via_bf16", "tf32_rn"]
 
 
 @pytest.mark.parametrize("mode", ALL_MODES)
