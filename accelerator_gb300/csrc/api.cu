@@ -202,8 +202,27 @@ int tc_launch(TcMode mode, const void* a_use, int64_t lda, const void* b_use, in
     // 32-byte chunks, the layout kind::tf32 reads such an operand in.
     const CUtensorMapSwizzle b_swizzle =
         es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-    if (rc == GEMM_OK)
+    // B in swizzle atoms ordered [k group][column block] (one 4-D box per
+    // stage) where the 4-D view covers B exactly, else in 2-D column boxes.
+    const bool b_atoms = tc_b_atoms(mode, K, N, ldb);
+    if (rc == GEMM_OK && b_atoms) {
+        const cuuint64_t dims[4] = {(cuuint64_t)shape.b_box_n, (cuuint64_t)shape.b_atom_rows,
+                                    (cuuint64_t)(N / shape.b_box_n),
+                                    (cuuint64_t)(K / shape.b_atom_rows)};
+        const cuuint64_t strides[3] = {(cuuint64_t)(N * es), (cuuint64_t)(shape.b_box_n * es),
+                                       (cuuint64_t)(N * es * shape.b_atom_rows)};
+        const cuuint32_t box[4] = {(cuuint32_t)shape.b_box_n, (cuuint32_t)shape.b_atom_rows,
+                                   (cuuint32_t)shape.b_blocks,
+                                   (cuuint32_t)(shape.k_elems / shape.b_atom_rows)};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        rc = g_encode(&map_b, dt, 4, const_cast<void*>(b_use), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, b_swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+                 ? GEMM_OK
+                 : GEMM_ERR_CUDA;
+    } else if (rc == GEMM_OK) {
         rc = encode_2d(&map_b, b_use, es, K, N, ldb, shape.b_box_n, shape.k_elems, dt, b_swizzle);
+    }
     if (rc != GEMM_OK) return rc;
     const bool c_vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
     // C as a TMA store target (32 x 32 fp32 boxes) when its rows are 16-byte aligned
@@ -219,7 +238,7 @@ int tc_launch(TcMode mode, const void* a_use, int64_t lda, const void* b_use, in
                        CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
         if (rc != GEMM_OK) return rc;
         if (launch_tc_gemm_pair(mode, map_a, map_b, mc, &map_w, C, (int)M, (int)N, (int)K, c_vec,
-                                epi, split, st->err, kWaitLimitNs, stream) != cudaSuccess)
+                                epi, split, b_atoms, st->err, kWaitLimitNs, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         g_launches++;
         if (launch_tc_tile_reduce(static_cast<const float*>(ws), split, C, (int)M, (int)N, c_vec,
@@ -230,7 +249,7 @@ int tc_launch(TcMode mode, const void* a_use, int64_t lda, const void* b_use, in
     }
     const cudaError_t e =
         pairs ? launch_tc_gemm_pair(mode, map_a, map_b, mc, nullptr, C, (int)M, (int)N, (int)K,
-                                    c_vec, epi, kNoSplit, st->err, kWaitLimitNs, stream)
+                                    c_vec, epi, kNoSplit, b_atoms, st->err, kWaitLimitNs, stream)
               : launch_tc_gemm(mode, map_a, map_b, C, (int)M, (int)N, (int)K, c_vec, epi,
                                st->num_sms, st->err, kWaitLimitNs, stream);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;

@@ -85,15 +85,21 @@ struct TcShape {
     int block_m, block_n;   // output tile per CTA
     int k_elems;            // K elements per pipeline stage (128 bytes)
     int b_box_n;            // N extent of one TMA box of B (128 bytes)
+    int b_atom_rows;        // k-rows per swizzle atom of B (4 TF32, 8 BF16/FP16)
+    int b_blocks;           // B column blocks (of b_box_n) per CTA of a pair
 };
 TcShape tc_shape(TcMode mode);
 cudaError_t tc_setup();
 // Clusters of two CTAs of the 2-SM kernel that fit at once (0: unavailable).
 int tc_max_pairs();
 // 2-SM (CTA pair) kernel, B read MN-major in every mode.  Its TMA boxes: A
-// as for the 1-SM kernel (block_m rows x 128 bytes); B boxes of k_elems rows
-// x 128 bytes (b_box_n columns), 128-byte swizzle of 16-byte chunks for
-// 16-bit elements and of 32-byte chunks for TF32.
+// as for the 1-SM kernel (block_m rows x 128 bytes); B, 128-byte swizzle of
+// 16-byte chunks for 16-bit elements and of 32-byte chunks for TF32, either
+// as 2-D boxes of k_elems rows x 128 bytes (b_box_n columns), or with
+// b_atoms as one 4-D box per stage over the view (b_box_n columns, b_atom_rows
+// k-rows, N / b_box_n column blocks, K / b_atom_rows k groups) of B, box
+// (b_box_n, b_atom_rows, b_blocks, k_elems / b_atom_rows): each MMA's B
+// operand then lies in one piece (tc_b_atoms says when that form applies).
 // map_c (may be null): C as a 2-D fp32 tensor, box 32 x 32, 128-byte swizzle,
 // for TMA stores of the epilogue; without it C is stored by the threads.
 // K split of the pair kernel: the first whole_tiles pair tiles (in the
@@ -122,8 +128,13 @@ int64_t tc_split_workspace_bytes(const TcSplit& split, int64_t M, int64_t N);
 cudaError_t launch_tc_gemm_pair(TcMode mode, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c,
                                 const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
-                                const Epilogue& epi, const TcSplit& split, unsigned* err,
-                                uint64_t limit_ns, cudaStream_t stream);
+                                const Epilogue& epi, const TcSplit& split, bool b_atoms,
+                                unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+// Whether the pair kernel reads B (row stride ldb elements) in the
+// atom-ordered 4-D form: pairs available, B read in place with N a multiple
+// of b_box_n and K of b_atom_rows (so the 4-D view covers B exactly), and not
+// disabled by GEMM_FORCE_CONFIG=b_boxes_2d.
+bool tc_b_atoms(TcMode mode, int64_t K, int64_t N, int64_t ldb);
 // C := the epilogue applied to the sum, in split order, of the workspace
 // blocks of every split tile (the whole tiles are left as they are).
 cudaError_t launch_tc_tile_reduce(const float* ws, const TcSplit& split, float* C, int M, int N,

@@ -70,6 +70,7 @@ struct Traits<TcMode::kBF16> {
     // MN-major B: 128-byte swizzle of 16-byte chunks, repeating every 8
     // k-rows (1024 bytes), the stride byte offset between 8-row groups.
     static constexpr uint32_t kBMnLayout = kLayoutSw128, kBMnSbo = 1024;
+    static constexpr int kAtomRows = 8;   // k-rows per swizzle atom (8 x 128 bytes)
 };
 template <>
 struct Traits<TcMode::kF16> {
@@ -77,6 +78,7 @@ struct Traits<TcMode::kF16> {
     static constexpr uint32_t kFormat = 0;       // F16
     static constexpr TcKind kKind = TcKind::kF16;
     static constexpr uint32_t kBMnLayout = kLayoutSw128, kBMnSbo = 1024;
+    static constexpr int kAtomRows = 8;
 };
 template <>
 struct Traits<TcMode::kTF32> {
@@ -89,6 +91,7 @@ struct Traits<TcMode::kTF32> {
     // k-rows: 512 bytes between 4-row groups.  (With the 16-byte-chunk
     // swizzle an MN-major kind::tf32 operand reads as zeros.)
     static constexpr uint32_t kBMnLayout = kLayoutSw128Atom32, kBMnSbo = 512;
+    static constexpr int kAtomRows = 4;   // k-rows per swizzle atom (4 x 128 bytes)
 };
 
 struct Sched {
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap map_c,
                         const __grid_constant__ CUtensorMap map_w, float* __restrict__ C, int M,
                         int N, int K, int pairs_m, int tiles_n, int c_mode, const Epilogue epi,
-                        int splits, int k_per_split, int whole_tiles, unsigned* err,
+                        int splits, int k_per_split, int whole_tiles, int b_4d, unsigned* err,
                         uint64_t limit_ns) {
     using T = Traits<MODE>;
     constexpr int kKElems = kSlabBytes / T::kEs;          // K per stage: 64 bf16 / 32 tf32
@@ -396,6 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBoxN = kSlabBytes / T::kEs;            // N per MN-major B box: 64 (bf16)
     constexpr int kBoxes = kPHalfN / kBoxN;               // 2 (bf16)
     constexpr uint32_t kBoxBytes = kKElems * kSlabBytes;  // 8 KB (bf16)
+    // The other B layout (b_4d): swizzle atoms of kAtomRows k-rows x 128
+    // bytes ordered [k group][column block], so that the B operand of one
+    // MMA (kUmmaK rows of all kBoxes column blocks) is 4 KB in one piece;
+    // one 4-D TMA box per stage writes it.  Leading byte offset = one atom
+    // (the next column block), stride byte offset = kBoxes atoms (the next
+    // k group).
+    constexpr uint32_t kAtomBytes = T::kAtomRows * kSlabBytes;            // 512 / 1024
+    constexpr uint32_t kKGroupBytes = kBoxes * kAtomBytes;                // 2 KB
+    constexpr uint32_t kMmaBBytes = (kUmmaK / T::kAtomRows) * kKGroupBytes;   // 4 KB
     constexpr uint32_t kIdesc = make_idesc(T::kFormat, 2 * kBM, kBN, false, true);
     constexpr uint32_t kPairTx = 2u * kPStageBytes;       // bytes the leader's full barrier awaits
 
@@ -493,10 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, kPairTx);
                     const uint32_t fb = full_leader0 + 8 * stage;
                     tma_load_2d_pair(sA + stage * kPABytes, &map_a, fb, kb * kKElems, my_m0);
+                    if (b_4d) {
+                        tma_load_4d_pair(sB + stage * kPBBytes, &map_b, fb, 0, 0, my_n0 / kBoxN,
+                                         kb * (kKElems / T::kAtomRows));
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < kBoxes; ++j)
-                        tma_load_2d_pair(sB + stage * kPBBytes + j * kBoxBytes, &map_b, fb,
-                                         my_n0 + j * kBoxN, kb * kKElems);
+                        for (int j = 0; j < kBoxes; ++j)
+                            tma_load_2d_pair(sB + stage * kPBBytes + j * kBoxBytes, &map_b, fb,
+                                             my_n0 + j * kBoxN, kb * kKElems);
+                    }
                     used[stage] = true;
                     last_phase[stage] = phase;
                     if (++stage == kPStages) stage = 0, phase ^= 1u;
@@ -538,8 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kMmaPerStage; ++kk) {
                         const uint64_t adesc = smem_desc_sw128(a_tile + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc(b_tile + kk * kUmmaK * kSlabBytes,
-                                                         kBoxBytes, T::kBMnSbo, T::kBMnLayout);
+                        const uint64_t bdesc =
+                            b_4d ? smem_desc(b_tile + kk * kMmaBBytes, kAtomBytes, kKGroupBytes,
+                                             T::kBMnLayout)
+                                 : smem_desc(b_tile + kk * kUmmaK * kSlabBytes, kBoxBytes,
+                                             T::kBMnSbo, T::kBMnLayout);
                         tc_mma_pair<T::kKind>(d_tmem, adesc, bdesc, kIdesc,
                                               (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
@@ -700,8 +720,10 @@ __global__ void __launch_bounds__(256)
 
 TcShape tc_shape(TcMode mode) {
     const int es = mode == TcMode::kTF32 ? 4 : 2;
-    return TcShape{kBM, kBN, kSlabBytes / es, kSlabBytes / es};
+    return TcShape{kBM, kBN, kSlabBytes / es, kSlabBytes / es, mode == TcMode::kTF32 ? 4 : 8,
+                   kPHalfN / (kSlabBytes / es)};
 }
+
 
 template <TcMode MODE>
 static cudaError_t set_attr() {
@@ -717,6 +739,14 @@ static cudaError_t set_pair_attr() {
 
 // Clusters of two that can be resident at once (0: pairs unavailable).
 static int g_max_pairs = 0;
+// GEMM_FORCE_CONFIG=b_boxes_2d: B always in the per-column-block layout.
+static bool g_force_b2d = false;
+
+bool tc_b_atoms(TcMode mode, int64_t K, int64_t N, int64_t ldb) {
+    const TcShape s = tc_shape(mode);
+    return g_max_pairs > 0 && !g_force_b2d && ldb == N && N % s.b_box_n == 0 &&
+           K % s.b_atom_rows == 0;
+}
 
 template <TcMode MODE>
 static int query_max_pairs(int num_sms) {
@@ -757,6 +787,7 @@ cudaError_t tc_setup() {
     // (it is otherwise only taken on devices that cannot hold pair clusters).
     const char* force = std::getenv("GEMM_FORCE_CONFIG");
     if (force && std::strcmp(force, "single_cta") == 0) g_max_pairs = 0;
+    g_force_b2d = force && std::strcmp(force, "b_boxes_2d") == 0;
     return cudaSuccess;
 }
 
@@ -817,8 +848,8 @@ TcSplit tc_plan_split(TcMode mode, int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_tc_gemm_pair(TcMode mode, const CUtensorMap& map_a,
                                 const CUtensorMap& map_b, const CUtensorMap* map_c,
                                 const CUtensorMap* map_w, float* C, int M, int N, int K, bool c_vec,
-                                const Epilogue& epi, const TcSplit& split, unsigned* err,
-                                uint64_t limit_ns, cudaStream_t stream) {
+                                const Epilogue& epi, const TcSplit& split, bool b_atoms,
+                                unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
     const int pairs_m = (M + 2 * kBM - 1) / (2 * kBM), tiles_n = (N + kBN - 1) / kBN;
     const int64_t pairs = (int64_t)pairs_m * tiles_n;
     if (pairs <= 0) return cudaSuccess;
@@ -850,16 +881,17 @@ cudaError_t launch_tc_gemm_pair(TcMode mode, const CUtensorMap& map_a,
     const CUtensorMap& mc = map_c ? *map_c : map_a;   // unused unless cm == kStoreTma
     const CUtensorMap& mw = map_w ? *map_w : map_a;   // unused without split units
     const int kps = splitting ? split.k_per_split : 0, wt = (int)whole;
+    const int b4 = b_atoms ? 1 : 0;
     cudaError_t e;
     if (mode == TcMode::kBF16)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kBF16>, map_a, map_b, mc, mw, C, M,
-                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, b4, err, limit_ns);
     else if (mode == TcMode::kTF32)
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kTF32>, map_a, map_b, mc, mw, C, M,
-                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, b4, err, limit_ns);
     else
         e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<TcMode::kF16>, map_a, map_b, mc, mw, C, M,
-                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, err, limit_ns);
+                               N, K, pairs_m, tiles_n, cm, epi, sp, kps, wt, b4, err, limit_ns);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -610,23 +610,28 @@ def run_sweep(args):
     torch.cuda.set_device(0)
     build.build()
     dev = torch.device("cuda", 0)
-    _, bf16_peak, _, src = _measured_peaks()
-    peaks = {"fp32": (fp32_ffma_peak(SM_MAX_MHZ, device_sms(dev)), "alu"),
-             "tf32": (bf16_peak * TF32_PER_BF16, "tensor"),
-             "bf16": (bf16_peak, "tensor")}
+    _, bf16_peak, bf16_sustained, src = _measured_peaks()
+    tensor_rate = {"tf32": TF32_PER_BF16, "tf32_rn": TF32_PER_BF16, "bf16": 1.0, "fp16": 1.0,
+                   "fp32_via_bf16": 1.0}
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     rows = []
+    sampler = ClockSampler(0)
+    sampler.__enter__()
     for n in (128, 256, 512, 1024, 2048, 4096, 8192):
         A, B = inputs.matrices(n, n, n, "u01")
         a32, b32 = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
         a16 = torch.from_numpy(inputs.bf16_bits(A).view(np.int16)).view(torch.bfloat16).to(dev)
         b16 = torch.from_numpy(inputs.bf16_bits(B).view(np.int16)).view(torch.bfloat16).to(dev)
+        h16 = None
+        if "fp16" in args.modes:
+            h16 = (torch.from_numpy(inputs.fp16_bits(A).view(np.int16)).view(torch.float16).to(dev),
+                   torch.from_numpy(inputs.fp16_bits(B).view(np.int16)).view(torch.float16).to(dev))
         C = torch.zeros((n, n), dtype=torch.float32, device=dev)
         for m in args.modes:
             if n > 4096 and m == "fp32":
                 continue
-            a, b = (a16, b16) if m == "bf16" else (a32, b32)
+            a, b = (a16, b16) if m == "bf16" else h16 if m == "fp16" else (a32, b32)
             mode = binding.MODES[m]
             times = []
             for r in range(args.warmup + args.steps):
@@ -642,13 +647,21 @@ def run_sweep(args):
                 raise RuntimeError(f"a kernel reported a timeout at N={n} {m}")
             ms = float(np.median(times))
             tf = flops(n, n, n) / (ms / 1e3) / 1e12
-            peak, bound = peaks[m]
-            rows.append({"n": n, "mode": m, "ms_median": ms, "tflops": tf, "bound": bound,
-                         "peak": peak, "frac": tf / peak})
-        del a32, b32, a16, b16, C
+            row = {"n": n, "mode": m, "ms_median": ms, "tflops": tf}
+            if m == "fp32":
+                row.update(bound="alu", peak=fp32_ffma_peak(SM_MAX_MHZ, device_sms(dev)))
+            else:
+                row.update(bound="tensor", peak=bf16_peak * tensor_rate[m])
+                if bf16_sustained:   # the power-capped loop's figure, for context
+                    row["frac_sustained"] = tf / (bf16_sustained * tensor_rate[m])
+            row["frac"] = tf / row["peak"]
+            rows.append(row)
+        del a32, b32, a16, b16, h16, C
         torch.cuda.empty_cache()
+    sampler.__exit__(None, None, None)
     print(json.dumps({"sweep": rows, "unit": UNIT, "peak_source": src, "warmup": args.warmup,
                       "repeats": args.steps, "l2": "flushed before every launch",
+                      "clocks": sampler.summary(),
                       "data": "synthetic U[0,1), seed 42"}), flush=True)
     return 0
 

@@ -23,9 +23,11 @@
  *
  * Environment (testing and tuning only; read once per process): with
  * GEMM_FORCE_CONFIG=single_cta the tensor-core modes use the 1-SM kernel even
- * where 2-SM clusters fit; =ffma_small / =ffma_tiles128 make every GEMM_FP32
- * product take the 32 x 32-tile or the 128 x 128-tile FFMA kernel instead of
- * the one chosen by shape.  Results stay within each mode's tolerance.
+ * where 2-SM clusters fit; =b_boxes_2d makes them load B by 2-D boxes per
+ * column block even where the atom-ordered 4-D form applies (same results,
+ * bit for bit); =ffma_small / =ffma_tiles128 make every GEMM_FP32 product
+ * take the 32 x 32-tile or the 128 x 128-tile FFMA kernel instead of the one
+ * chosen by shape.  Results stay within each mode's tolerance.
  */
 #ifndef LIBGEMM_GEMM_H
 #define LIBGEMM_GEMM_H
