@@ -1,5 +1,5 @@
 """Seeded random products: shapes up to 3000 (K up to 6000 when M*N is
-small), all five modes, random alpha and beta, and operands and C placed at
+small), all six modes, random alpha and beta, and operands and C placed at
 element offsets 0..2 inside larger buffers, so bases that are aligned to the
 element but not to 16 bytes are covered along with every split and edge
 path the shapes happen to take.  Each result is compared with the oracle
