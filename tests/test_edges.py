@@ -16,7 +16,7 @@ from gpu_util import device_operands, run
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["fp32", "tf32", "bf16", "fp16"]
+MODES = ["fp32", "tf32", "bf16", "fp16", "tf32_rn"]
 DIMS = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 63, 65, 127, 129, 255, 257]
 
 

@@ -38,7 +38,7 @@ def large_case():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp16"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp16", "tf32_rn"])
 def test_operand_beyond_2_31_elements(libgemm, large_case, mode):
     import torch
     a32, b32, Cref = large_case
