@@ -159,6 +159,20 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
         }
         ws = static_cast<float*>(scratch);
     }
+    if (plan.stream) {   // partial tiles, then the per-tile counters (zeroed)
+        const int64_t wb = round_up(plan.ws_bytes, 256), cb = round_up(plan.counter_bytes, 256);
+        if (cudaMallocFromPoolAsync(&scratch, (size_t)(wb + cb), st->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NO_MEMORY;
+        }
+        ws = static_cast<float*>(scratch);
+        counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(scratch) + wb);
+        if (launch_fill_zero(reinterpret_cast<float*>(counters), cb / 4, stream) != cudaSuccess) {
+            cudaFreeAsync(scratch, stream);
+            return GEMM_ERR_CUDA;
+        }
+        g_launches++;
+    }
     int rc = GEMM_OK;
     if (launch_ffma_sgemm(A, B, C, (int)M, (int)N, (int)K, b_vec, c_vec, plan, partial, counters,
                           epi, ws, stream) != cudaSuccess)
@@ -172,6 +186,7 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
         else
             g_launches++;
     }
+
     if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && rc == GEMM_OK) rc = GEMM_ERR_CUDA;
     return rc;
 }

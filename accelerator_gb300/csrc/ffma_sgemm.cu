@@ -34,6 +34,9 @@
 //     16 rows and ~29 columns of tiles, ~90 MB of operands: DRAM reads per
 //     launch 271 MB, against 325 MB with groups of 8 and 472 MB with 32;
 //     the time is the same, the kernel being bound by its FMA pipe).
+#include <cstdlib>
+#include <cstring>
+
 #include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -380,13 +383,274 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     }
 }
 
+// ---- stream-K form: one persistent CTA per resident slot ----
+// For shapes whose tiles fill between half a wave and two waves of CTA
+// slots, whole tiles leave slots idle (2048^3: 256 tiles on 456 slots run as
+// 104 SMs with two CTAs and 48 with one) or a last wave partly empty.  Here
+// the space of tile x K-slab units (tiles in raster order, slabs ascending
+// within a tile) is cut into gridDim.x equal contiguous ranges, one per CTA,
+// [total * b / G, total * (b + 1) / G).  A CTA walks its range tile by tile,
+// each tile as the FFMA chain over its slabs of the range (the loop of
+// ffma_sgemm_kernel); a tile it covers wholly is stored to C with the
+// epilogue; the first and the last tile of its range, when it covers only
+// part of them, store their raw partial sums to workspace blocks 2b and
+// 2b + 1 (kBM x kBN floats each) and count the piece on the tile's counter;
+// the CTA that stores a tile's last piece (in time) adds all of its pieces
+// in K order and stores C: C_ij is then ((p0 + p1) + p2), the same on every
+// run.  With at least half a wave of tiles a CTA's range is longer than
+// half a tile, so a tile has at most three pieces (kMaxPieces).
+
+// Tile coordinates in the grouped raster (kGroupM tile-rows per group).
+__device__ __forceinline__ void ffma_tile_coords(int tile, int tiles_m, int tiles_n, int& m0,
+                                                 int& n0) {
+    const int per_group = kGroupM * tiles_n;
+    const int group = tile / per_group;
+    const int first_m = group * kGroupM;
+    const int gsize = min(tiles_m - first_m, kGroupM);
+    m0 = (first_m + (tile % per_group) % gsize) * kBM;
+    n0 = ((tile % per_group) / gsize) * kBN;
+}
+
+// First unit of CTA b's range, and the CTA whose range holds unit x.
+__device__ __forceinline__ int64_t stream_lo(int64_t total, int64_t b, int64_t G) {
+    return total * b / G;
+}
+__device__ __forceinline__ int64_t stream_owner(int64_t total, int64_t x, int64_t G) {
+    return ((x + 1) * G - 1) / total;
+}
+
+constexpr int kMaxPieces = 3;
+
+template <class CF, bool kBVec, bool kCVec>
+__global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
+    ffma_stream_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                       float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
+                       float* __restrict__ ws, unsigned* __restrict__ counters,
+                       const Epilogue epi) {
+    constexpr int TM = CF::TM, TN = CF::TN, kStages = CF::kStages;
+    extern __shared__ __align__(16) float smem[];
+    float* sA = smem;
+    float* sB = smem + kStages * kAStage;
+    __shared__ unsigned s_last;
+
+    const int nkt = (K + kBK - 1) / kBK;
+    const int64_t G = gridDim.x;
+    const int64_t total = (int64_t)tiles_m * tiles_n * nkt;
+    const int64_t lo = stream_lo(total, blockIdx.x, G), hi = stream_lo(total, blockIdx.x + 1, G);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm0 = (warp / CF::kWarpsN) * CF::WM;
+    const int wn0 = (warp % CF::kWarpsN) * CF::WN;
+    const int lm = CF::kNMajor ? lane / CF::LN : lane % CF::LM;
+    const int ln = CF::kNMajor ? lane % CF::LN : lane / CF::LM;
+    const int am = wm0 + lm * 4;
+    const int bn = wn0 + ln * 4;
+    auto row_of = [&](int i) { return am + (i / 4) * (CF::LM * 4) + (i % 4); };
+    auto col_of = [&](int j) { return bn + (j / 4) * (CF::LN * 4) + (j % 4); };
+    const int full_slabs = K / kBK;
+#ifdef GEMM_DEBUG
+    const int64_t ws_bytes = G * 2 * (kBM * kBN) * 4;
+#endif
+
+    for (int64_t u = lo; u < hi;) {
+        const int tile = (int)(u / nkt);
+        const int kt_begin = (int)(u - (int64_t)tile * nkt);
+        const int kt_end = (int)(hi - u < (int64_t)(nkt - kt_begin) ? kt_begin + (hi - u) : nkt);
+        int m0, n0;
+        ffma_tile_coords(tile, tiles_m, tiles_n, m0, n0);
+
+        float2 acc2[TM / 2][TN];
+#pragma unroll
+        for (int p = 0; p < TM / 2; ++p)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc2[p][j] = make_float2(0.0f, 0.0f);
+        auto acc = [&](int i, int j) -> float& {
+            return (i & 1) ? acc2[i >> 1][j].y : acc2[i >> 1][j].x;
+        };
+
+        const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, m0, n0, tid);
+        const int nloc = kt_end - kt_begin;
+        const bool interior = m0 + kBM <= M && n0 + kBN <= N;
+        const int interior_end = interior ? full_slabs : 0;
+#pragma unroll
+        for (int s = 0; s < kStages - 1; ++s) {
+            if (s < nloc) {
+                const int kt = kt_begin + s;
+                if (kt < interior_end) loader.load_interior(kt, s);
+                else loader.load(kt, s, K, kt >= full_slabs);
+            }
+            cp_async_commit();
+        }
+        for (int i = 0; i < nloc; ++i) {
+            cp_async_wait<kStages - 2>();
+            __syncthreads();
+            {
+                const int nxt = i + kStages - 1;
+                if (nxt < nloc) {
+                    const int kt = kt_begin + nxt;
+                    if (kt < interior_end) loader.load_interior(kt, nxt % kStages);
+                    else loader.load(kt, nxt % kStages, K, kt >= full_slabs);
+                }
+                cp_async_commit();
+            }
+            const float* a_s = sA + (i % kStages) * kAStage;
+            const float* b_s = sB + (i % kStages) * kBStage;
+#pragma unroll
+            for (int k = 0; k < kBK; ++k) {
+                float2 a2[TM / 2];
+                float b[TN];
+#pragma unroll
+                for (int c = 0; c < TM / 4; ++c) {
+                    const float4 t =
+                        *reinterpret_cast<const float4*>(a_s + k * kLdA + am + c * CF::LM * 4);
+                    a2[2 * c] = make_float2(t.x, t.y), a2[2 * c + 1] = make_float2(t.z, t.w);
+                }
+#pragma unroll
+                for (int c = 0; c < TN / 4; ++c) {
+                    const float4 t =
+                        *reinterpret_cast<const float4*>(b_s + k * kLdB + bn + c * CF::LN * 4);
+                    b[4 * c] = t.x, b[4 * c + 1] = t.y, b[4 * c + 2] = t.z, b[4 * c + 3] = t.w;
+                }
+#pragma unroll
+                for (int j = 0; j < TN; ++j) {
+                    const float2 bj = make_float2(b[j], b[j]);
+#pragma unroll
+                    for (int pp = 0; pp < TM / 2; ++pp)
+                        acc2[pp][j] = __ffma2_rn(a2[pp], bj, acc2[pp][j]);
+                }
+            }
+        }
+        cp_async_wait<0>();
+
+        if (kt_begin == 0 && kt_end == nkt) {
+            // the whole tile in this range: C, with the epilogue, guarded
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const int row = m0 + row_of(i);
+                if (row >= M) continue;
+                float* crow = C + (int64_t)row * N;
+#pragma unroll
+                for (int h = 0; h < TN / 4; ++h) {
+                    const int col = n0 + col_of(4 * h);
+                    if (kCVec && col < N) {
+                        if (!GEMM_DBG_OK(crow + col, C, (int64_t)M * N * 4, 16)) continue;
+                        *reinterpret_cast<float4*>(crow + col) = epilogue_apply4(
+                            epi,
+                            make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2),
+                                        acc(i, 4 * h + 3)),
+                            crow + col);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (col + j < N && GEMM_DBG_OK(crow + col + j, C, (int64_t)M * N * 4, 4))
+                                crow[col + j] = epilogue_apply(epi, acc(i, 4 * h + j), crow + col + j);
+                    }
+                }
+            }
+        } else {
+            // a piece: the raw partial of the whole kBM x kBN block
+            float* blk = ws + ((int64_t)blockIdx.x * 2 + (u == lo ? 0 : 1)) * (kBM * kBN);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int h = 0; h < TN / 4; ++h) {
+                    float* p = blk + row_of(i) * kBN + col_of(4 * h);
+                    if (GEMM_DBG_OK(p, ws, ws_bytes, 16))
+                        *reinterpret_cast<float4*>(p) =
+                            make_float4(acc(i, 4 * h), acc(i, 4 * h + 1), acc(i, 4 * h + 2),
+                                        acc(i, 4 * h + 3));
+                }
+            // count the piece; the last one to arrive adds the tile's pieces
+            const int64_t x0 = (int64_t)tile * nkt;
+            const int64_t b0 = stream_owner(total, x0, G), b1 = stream_owner(total, x0 + nkt - 1, G);
+            const int npieces = (int)(b1 - b0 + 1);
+            __threadfence();
+            __syncthreads();
+            // the counters' zero fill (the launch before this one, which may
+            // still run: programmatic stream serialisation) is complete and visible
+            grid_dependency_wait();
+            if (tid == 0)
+                s_last = GEMM_DBG_OK(counters + tile, counters, (int64_t)tiles_m * tiles_n * 4, 4) &&
+                         atomicAdd(counters + tile, 1u) == (unsigned)(npieces - 1);
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                // the pieces' blocks in K order: the tile is the first piece of
+                // CTA b's range unless that range began before it
+                const float* pb[kMaxPieces];
+#pragma unroll
+                for (int q = 0; q < kMaxPieces; ++q) {
+                    const int64_t b = b0 + q < b1 ? b0 + q : b1;
+                    pb[q] = ws + (2 * b + (b == b0 && stream_lo(total, b, G) < x0 ? 1 : 0)) *
+                                     (int64_t)(kBM * kBN);
+                }
+                // eight fragments at a time, every piece's loads issued before the
+                // adds (pieces beyond kMaxPieces, which the planner's range rules
+                // out, are added one by one after them, still in K order)
+#pragma unroll
+                for (int f0 = 0; f0 < TM * (TN / 4); f0 += 8) {
+                    float4 v[kMaxPieces][8];
+#pragma unroll
+                    for (int q = 0; q < kMaxPieces; ++q)
+#pragma unroll
+                        for (int f = 0; f < 8; ++f) {
+                            const int i = (f0 + f) / (TN / 4), h = (f0 + f) % (TN / 4);
+                            const float* p = pb[q] + row_of(i) * kBN + col_of(4 * h);
+                            v[q][f] = q < npieces && GEMM_DBG_OK(p, ws, ws_bytes, 16)
+                                          ? __ldcg(reinterpret_cast<const float4*>(p))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                    for (int f = 0; f < 8; ++f) {
+                        const int i = (f0 + f) / (TN / 4), h = (f0 + f) % (TN / 4);
+                        float4 sum = v[0][f];
+#pragma unroll
+                        for (int q = 1; q < kMaxPieces; ++q)
+                            if (q < npieces)
+                                sum.x += v[q][f].x, sum.y += v[q][f].y, sum.z += v[q][f].z,
+                                    sum.w += v[q][f].w;
+                        for (int64_t b = b0 + kMaxPieces; b <= b1; ++b) {
+                            const float* p =
+                                ws + 2 * b * (int64_t)(kBM * kBN) + row_of(i) * kBN + col_of(4 * h);
+                            if (!GEMM_DBG_OK(p, ws, ws_bytes, 16)) continue;
+                            const float4 w = __ldcg(reinterpret_cast<const float4*>(p));
+                            sum.x += w.x, sum.y += w.y, sum.z += w.z, sum.w += w.w;
+                        }
+                        const int row = m0 + row_of(i), col = n0 + col_of(4 * h);
+                        if (row >= M) continue;
+                        float* crow = C + (int64_t)row * N;
+                        if (kCVec && col < N) {
+                            if (GEMM_DBG_OK(crow + col, C, (int64_t)M * N * 4, 16))
+                                *reinterpret_cast<float4*>(crow + col) =
+                                    epilogue_apply4(epi, sum, crow + col);
+                        } else {
+                            const float a[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (col + j < N &&
+                                    GEMM_DBG_OK(crow + col + j, C, (int64_t)M * N * 4, 4))
+                                    crow[col + j] = epilogue_apply(epi, a[j], crow + col + j);
+                        }
+                    }
+                }
+            }
+        }
+        u += nloc;
+        __syncthreads();   // every warp is done with the ring before the next tile refills it
+    }
+}
+
 template <bool BV, bool CV>
 cudaError_t set_smem_attr() {
     cudaError_t e = cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FfmaCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV, true>,
+    e = cudaFuncSetAttribute(ffma_sgemm_kernel<FfmaCfg, BV, CV, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FfmaCfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(ffma_stream_kernel<FfmaCfg, BV, CV>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)FfmaCfg::kSmemBytes);
 }
@@ -442,10 +706,44 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
             return p;
         }
     }
+    // Between half a wave and two waves of tiles, with K long enough that a
+    // CTA's range holds at least kMinStreamSlabs slabs: stream-K, one
+    // persistent CTA per slot (GEMM_FORCE_CONFIG=ffma_no_stream disables it).
+    // Under one wave it is always taken (whole tiles leave slots idle: 2048^3
+    // 365 -> 309 us, 2432^3 603 -> 498 us).  From one to two waves it is
+    // taken when its cost in slab times, an equal share plus kStreamCost
+    // (restarts and the partial tiles), is under 97 % of a full wave plus the
+    // last wave as split below (its pieces plus kSplitCost): measured 3072^3
+    // 1069 -> 977 us and 3584^3 1694 -> 1528 us taken; 2944^3 (tail split 6
+    // ways, 850 against 866 us) and 3840^3 (1.97 waves, 1815 against 1863 us)
+    // left as they were.
+    constexpr int64_t kMinStreamSlabs = 32, kStreamCost = 8, kSplitCost = 8, kMinSlabs = 8;
+    static const bool no_stream = [] {
+        const char* f = std::getenv("GEMM_FORCE_CONFIG");
+        return f && std::strcmp(f, "ffma_no_stream") == 0;
+    }();
+    const int64_t total = tiles * nkt;
+    bool stream_k = !no_stream && slots > 0 && 2 * tiles > slots && tiles < 2 * slots &&
+                    tiles % slots != 0 && total >= kMinStreamSlabs * slots;
+    if (stream_k && tiles > slots) {
+        int64_t s = slots / (tiles - slots);
+        if (s > nkt / kMinSlabs) s = nkt / kMinSlabs;
+        if (s > 16) s = 16;
+        const int64_t tail = s >= 2 ? (nkt + s - 1) / s + kSplitCost : nkt;
+        const int64_t cost = (total + slots - 1) / slots + kStreamCost;
+        stream_k = cost * 100 < (nkt + tail) * 97;
+    }
+    if (stream_k) {
+        p.stream = true;
+        p.stream_ctas = slots;
+        p.dp_tiles = 0;
+        p.ws_bytes = p.stream_ctas * 2 * kBM * kBN * (int64_t)sizeof(float);   // two blocks a CTA
+        p.counter_bytes = tiles * (int64_t)sizeof(unsigned);                    // one a tile
+        return p;
+    }
     // Split the tiles of a partial last wave (after at least one full wave)
     // along K, as many ways as still fit in one wave, keeping at least
     // kMinSlabs slabs per piece; the last piece of a tile adds them up.
-    constexpr int64_t kMinSlabs = 8;
     if (rem > 0 && tiles > slots) {
         int64_t s = slots / rem;
         if (s > nkt / kMinSlabs) s = nkt / kMinSlabs;
@@ -483,6 +781,37 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
                               cudaStream_t stream) {
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     if (plan.tiles <= 0) return cudaSuccess;
+    if (plan.stream) {
+        if (!ws || !counters || plan.stream_ctas <= 0 || plan.stream_ctas > 0x7FFFFFFF)
+            return cudaErrorInvalidValue;
+        // Programmatic stream serialisation: the CTAs start while the zero
+        // fill of the counters before them finishes; everything they read
+        // before their first counter update (A, B) was written before it.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)plan.stream_ctas);
+        cfg.blockDim = dim3(FfmaCfg::kThreads);
+        cfg.dynamicSmemBytes = FfmaCfg::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = kUsePdl ? 1 : 0;
+        cudaError_t e;
+        if (b_vec && c_vec)
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, true>, A, B, C, M, N, K,
+                                   tiles_m, tiles_n, ws, counters, epi);
+        else if (b_vec)
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, false>, A, B, C, M, N, K,
+                                   tiles_m, tiles_n, ws, counters, epi);
+        else if (c_vec)
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, false, true>, A, B, C, M, N, K,
+                                   tiles_m, tiles_n, ws, counters, epi);
+        else
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, false, false>, A, B, C, M, N,
+                                   K, tiles_m, tiles_n, ws, counters, epi);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const int64_t ctas = plan.dp_tiles + plan.split_tiles * plan.splits;
     if (ctas > 0x7FFFFFFF || (plan.wide && !ws)) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)ctas);

@@ -54,12 +54,18 @@ __device__ __forceinline__ float4 epilogue_apply4(const Epilogue& e, float4 acc,
 // Wide plan (wide = true): every tile is split; the pieces store their raw
 // partials into ws_bytes of workspace (splits blocks of M x N floats) and
 // launch_splitk_reduce adds them and applies the epilogue.
+// Stream-K plan (stream = true): stream_ctas persistent CTAs share the tile x
+// K-slab units equally; ws_bytes of workspace hold two partial tiles per CTA,
+// and counter_bytes of counters (one per tile, zeroed before the launch) let
+// the last piece of a split tile add the pieces up (`counters` argument).
 struct FfmaPlan {
     int64_t tiles, dp_tiles, split_tiles;
     int splits;
     int64_t partial_bytes, counter_bytes;
     bool wide;
     int64_t ws_bytes;
+    bool stream;
+    int64_t stream_ctas;
 };
 cudaError_t ffma_setup();
 FfmaPlan ffma_plan(int M, int N, int K, int num_sms);
@@ -67,6 +73,7 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
                               bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
                               unsigned* counters, const Epilogue& epi, float* ws,
                               cudaStream_t stream);
+
 
 // ---- small-product FFMA GEMM (ffma_small.cu) ----
 // Products with at most kSmallMaxMN outputs and K <= kSmallMaxK take the

@@ -165,6 +165,10 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __r
 }
 
 __global__ void fill_zero_kernel(float* __restrict__ C, int64_t n) {
+    // a kernel launched after this one with programmatic stream serialisation
+    // (the FFMA stream-K kernel) may start at once; it waits for the zeros
+    // before it reads them
+    grid_launch_dependents();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
         if (GEMM_DBG_OK(C + i, C, n * 4, 4)) C[i] = 0.0f;

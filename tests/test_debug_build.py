@@ -7,7 +7,7 @@ CPU: both variants build and say which they are.  GPU: a child process loads
 the debug build and runs products along every kernel path -- FFMA interior
 and edge tiles, the in-kernel split of a partial last wave and the workspace
 split, the tensor kernels whole, with the last round split and all split,
-the 1-SM fallback, the small-product FFMA kernel, the re-stride and the
+the 1-SM fallback, the small-product FFMA kernel, the FFMA stream-K form, the re-stride and the
 bfloat16 and TF32 rounding passes, the alpha / beta update and K = 0 -- each checked
 against the oracle, with no bounds report after any of them."""
 import ctypes
@@ -86,6 +86,10 @@ else:
         check("fp32", *shp)
     check("fp32", 2816, 256, 2816, sampled=True)
     check("fp32", 1000, 777, 1500, alpha=0.5, beta=-1.25)
+    # FFMA stream-K (a persistent CTA per slot, a split tile's pieces added
+    # by the CTA of its last piece): vector and scalar B and C
+    check("fp32", 2000, 1601, 2100, sampled=True)
+    check("fp32", 1990, 1601, 2102, sampled=True, alpha=0.5, beta=-1.25)
     # tensor kernels: re-strided A (K % 4 != 0), re-strided B and scalar
     # stores (N % 4 != 0),
     # all tiles split (one pair tile, long K), the last round split
@@ -120,7 +124,7 @@ def _child(env_extra):
 @pytest.mark.gpu
 def test_debug_build_all_paths_in_bounds():
     out = _child({})
-    assert out.count("ok ") == 30
+    assert out.count("ok ") == 32
 
 
 @pytest.mark.gpu

@@ -115,8 +115,9 @@ def test_large_8192_sampled(libgemm, mode):
 def test_fp32_is_the_binary32_fma_chain(libgemm, M, K, N):
     """FP32 mode, bit for bit: each C_ij is acc = fma(A_ik, B_kj, acc), k
     ascending, wherever the library keeps a tile's K range whole: K < 128
-    (under 8 slabs of 16), or a tile count of half a wave or more that does
-    not exceed one wave (2048^2: 256 tiles of 128 x 128)."""
+    (under 8 slabs of 16), or a tile count between half a wave and two waves
+    with fewer than 32 slabs per CTA of the stream-K form (2048 x 240 x 2048:
+    256 tiles of 128 x 128, 15 slabs each)."""
     A, B = inputs.matrices(M, K, N, "pm1", seed=M + 7 * K + 13 * N)
     C = run(libgemm, A, B, "fp32")
     np.testing.assert_array_equal(C, oracle.fma_chain(A, B))
