@@ -5,7 +5,9 @@ The library's per-device set-up happens at the first call on a device, so
 each test makes one eager call before capturing.  Captured shapes include
 ones that take scratch from the library's stream-ordered pool inside the
 capture (the re-strided A of K = 777, the BF16 rounding pass, the K-split
-workspaces) and so become graph memory nodes.
+workspaces, the FFMA stream-K form's partial tiles and counters, whose zero
+fill the stream-K kernel follows by programmatic dependent launch) and so
+become graph memory nodes.
 """
 import numpy as np
 import pytest
@@ -19,7 +21,7 @@ CASES = [("fp32", 1000, 777, 1500), ("tf32", 1000, 777, 1500), ("bf16", 1000, 77
          ("fp16", 1000, 777, 1500), ("fp32_via_bf16", 1000, 777, 1500),
          ("tf32_rn", 1000, 777, 1500),
          ("bf16", 256, 16384, 256), ("tf32", 4096, 512, 4096), ("fp32", 256, 4096, 256),
-         ("fp32", 4096, 256, 4096)]
+         ("fp32", 4096, 256, 4096), ("fp32", 2048, 1024, 2048)]
 
 
 @pytest.mark.parametrize("mode,M,K,N", CASES, ids=lambda v: str(v))

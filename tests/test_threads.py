@@ -26,7 +26,8 @@ from gpu_util import device_operands, oracle_inputs
 torch.cuda.init()
 jobs = [("fp32", 300, 700, 200), ("tf32", 257, 130, 261), ("bf16", 1000, 777, 1500),
         ("fp16", 256, 8192, 256), ("fp32_via_bf16", 640, 96, 1028), ("tf32", 256, 16384, 256),
-        ("fp32", 128, 4096, 128), ("bf16", 512, 768, 1024), ("tf32_rn", 700, 512, 900)]
+        ("fp32", 128, 4096, 128), ("bf16", 512, 768, 1024), ("tf32_rn", 700, 512, 900),
+        ("fp32", 2048, 1024, 2048)]
 prepared = []
 for i, (mode, M, K, N) in enumerate(jobs):
     A, B = inputs.matrices(M, K, N, "pm1", seed=100 + i)
@@ -70,4 +71,4 @@ def test_concurrent_first_calls_and_streams():
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "ok 9" in r.stdout
+    assert "ok 10" in r.stdout
