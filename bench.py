@@ -461,6 +461,19 @@ E2E_GROUP_OF = {"fp32": "f32", "tf32": "f32", "fp32_via_bf16": "f32", "tf32_rn":
 E2E_GROUP_BYTES = {"f32": 4, "bf16": 2, "fp16": 2}
 
 
+# The order of an end-to-end step's products: the longest (FP32) last, so
+# that the other products' copies out overlap it and after the last step only
+# its C is still to copy; TF32 first, whose inputs are FP32's and so are
+# copied first.  Measured at 4096: 161.5 TFLOP/s against 159.5-159.9 with
+# FP32 first.
+E2E_RANK = {"tf32": 0, "tf32_rn": 1, "fp32_via_bf16": 2, "bf16": 3, "fp16": 4, "fp32": 9}
+
+
+def e2e_order(modes):
+    """The step's products in the order the end-to-end leg runs them."""
+    return tuple(sorted(modes, key=lambda m: E2E_RANK[m]))
+
+
 def e2e_input_groups(modes):
     """The input sets a step copies, once each, in the order its products
     first read them (so the first product waits only for its own inputs)."""
@@ -481,15 +494,17 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     step and shared by the products that take them (A and B as float32 serve
     FP32, TF32 and FP32_VIA_BF16, as on the device-timed leg).  The copy-in
     stream, the compute stream and the copy-out stream are ordered by events,
-    so a buffer is only overwritten after every earlier use has finished."""
+    so a buffer is only overwritten after every earlier use has finished.
+    The products run in e2e_order."""
     import torch
     from accelerator_gb300 import binding, inputs
     mode_ids = {"fp32": binding.FP32, "tf32": binding.TF32, "bf16": binding.BF16,
                 "fp16": binding.FP16, "fp32_via_bf16": binding.FP32_VIA_BF16,
                 "tf32_rn": binding.TF32_RN}
     group_of = E2E_GROUP_OF
+    modes = e2e_order(args.modes)
     host = {}
-    for g in e2e_input_groups(args.modes):
+    for g in e2e_input_groups(modes):
         if g == "f32":
             host[g] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), None)
         elif g == "bf16":
@@ -509,14 +524,14 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
                              xa=torch.empty(ha.shape, dtype=ha.dtype, device=dev),
                              xb=torch.empty(hb.shape, dtype=hb.dtype, device=dev),
                              loaded=torch.cuda.Event(), readers=[])
-        for m in args.modes:
+        for m in modes:
             outs[k][m] = dict(c=torch.empty((n, n), dtype=torch.float32, device=dev),
                               hc=torch.empty((n, n), dtype=torch.float32).pin_memory(),
                               done=torch.cuda.Event(), out=torch.cuda.Event(), used=False)
     h2d = sum(ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
               for ha, hb, _ in host.values())
-    d2h = len(args.modes) * n * n * 4
-    assert (h2d, d2h) == e2e_bytes_per_step(args.modes, n)
+    d2h = len(modes) * n * n * 4
+    assert (h2d, d2h) == e2e_bytes_per_step(modes, n)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     parity = [0]
 
@@ -530,7 +545,7 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
                 b["xb"].copy_(b["hb"], non_blocking=True)
                 b["loaded"].record(s_in)
             b["readers"] = []
-        for m in args.modes:
+        for m in modes:
             b, o = ins[k][group_of[m]], outs[k][m]
             stream.wait_event(b["loaded"])
             if o["used"]:
@@ -561,10 +576,11 @@ def run_e2e(args, A, B, n, dev, stream, ws, f):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)   # the slowest rank's
     if binding.debug_status(stream) != binding.OK:
         raise RuntimeError("a kernel reported a timeout during the end-to-end run")
-    return {"value": ws * len(args.modes) * f / (ms / 1e3) / 1e12, "unit": UNIT,
+    return {"value": ws * len(modes) * f / (ms / 1e3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "overlap": "copy-in, compute and copy-out on three streams; each input copied "
-                       "once per step and shared by the modes that read it"}
+                       "once per step and shared by the modes that read it; products in the "
+                       "order " + ",".join(modes) + " (the longest last)"}
 
 
 def _cpu_model() -> str:

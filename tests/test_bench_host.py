@@ -49,6 +49,11 @@ def test_e2e_input_sets():
     assert bench.e2e_input_groups(("bf16", "fp32")) == ["bf16", "f32"]
     assert bench.e2e_input_groups(bench.ALL_MODES) == ["f32", "bf16", "fp16"]
     assert bench.e2e_input_groups(("tf32", "fp32_via_bf16")) == ["f32"]
+    # the end-to-end step runs FP32, the longest product, last
+    assert bench.e2e_order(bench.MODES) == ("tf32", "bf16", "fp32")
+    assert bench.e2e_order(bench.ALL_MODES)[-1] == "fp32"
+    assert sorted(bench.e2e_order(bench.ALL_MODES)) == sorted(bench.ALL_MODES)
+    assert bench.e2e_input_groups(bench.e2e_order(bench.MODES)) == ["f32", "bf16"]
     # 4096^2: 2 x 64 MiB float32 + 2 x 32 MiB bfloat16 in, 3 x 64 MiB out
     h2d, d2h = bench.e2e_bytes_per_step(bench.MODES, 4096)
     assert h2d == 201326592 and d2h == 201326592
