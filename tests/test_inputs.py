@@ -48,6 +48,37 @@ def test_bf16_round_to_nearest_even():
     assert abs(float(back[0]) / 3.0e38 - 1) < 2.0 ** -8
 
 
+def _bf16_nearest_even_by_definition(x):
+    """The bfloat16 value nearest to each float32 x, ties to the even
+    significand, found from the two neighbouring bfloat16 values (the
+    truncation and the next one up in magnitude) compared in float64, where
+    both distances are exact: no rounding trick on the bit pattern."""
+    u = x.view(np.uint32)
+    lo = (u & np.uint32(0xFFFF0000))                     # toward zero
+    hi = lo + np.uint32(0x10000)                         # next in magnitude
+    flo = lo.view(np.float32).astype(np.float64)
+    fhi = hi.view(np.float32).astype(np.float64)
+    fx = x.astype(np.float64)
+    dlo, dhi = np.abs(fx - flo), np.abs(fhi - fx)
+    even_lo = ((lo >> np.uint32(16)) & np.uint32(1)) == 0
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ~even_lo)
+    return np.where(pick_hi, hi, lo) >> np.uint32(16)
+
+
+def test_bf16_matches_nearest_even_definition():
+    rng = np.random.default_rng(11)
+    # finite patterns whose next bfloat16 up is still finite
+    u = rng.integers(0, 0x7F7F0000, size=200000, dtype=np.uint64).astype(np.uint32)
+    ties = (u & np.uint32(0xFFFF0000)) | np.uint32(0x8000)          # exactly halfway
+    carries = np.uint32(0x3F80FFFF) + np.zeros(1, np.uint32)        # rounds into the next binade
+    subnormal = rng.integers(1, 0x007FFFFF, size=2000, dtype=np.uint64).astype(np.uint32)
+    u = np.concatenate([u, ties, carries, subnormal, np.array([0x3FFF8000, 0x3FFFFFFF], np.uint32)])
+    u = np.concatenate([u, u | np.uint32(0x80000000)])              # and the negatives
+    x = u.view(np.float32)
+    got = inputs.bf16_bits(x).astype(np.uint32)
+    np.testing.assert_array_equal(got, _bf16_nearest_even_by_definition(x))
+
+
 def test_tf32_rna_recipe_matches_the_oracle_format():
     """The host-side TF32 rounding recipe (a bit trick) and the oracle's
     format (the grid definition) agree on finite values, ties included."""
