@@ -20,17 +20,35 @@
 namespace libgemm {
 namespace {
 
-template <typename T>
-__global__ void restride_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows,
-                                int64_t cols, int64_t src_ld, int64_t dst_ld) {
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const T* s = src + r * src_ld;
-        T* d = dst + r * dst_ld;
-        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cols;
-             c += (int64_t)gridDim.x * blockDim.x)
-            if (GEMM_DBG_OK(s + c, src, ((rows - 1) * src_ld + cols) * (int64_t)sizeof(T), sizeof(T)) &&
-                GEMM_DBG_OK(d + c, dst, rows * dst_ld * (int64_t)sizeof(T), sizeof(T)))
-                d[c] = s[c];
+// Rows of row_bytes bytes from stride src_ld to stride dst_ld (both in
+// bytes), copied V bytes at a time -- V the widest unit that divides both
+// bases and both strides -- and the rows' last row_bytes % V bytes two at a
+// time (elements are 2 or 4 bytes).  One flat index runs over all (row,
+// unit) pairs, so consecutive threads copy consecutive units and every
+// thread has several independent copies in flight.
+template <typename V>
+__global__ void restride_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                int64_t rows, int64_t row_bytes, int64_t src_ld, int64_t dst_ld) {
+    const int64_t nvec = row_bytes / (int64_t)sizeof(V), tail0 = nvec * (int64_t)sizeof(V);
+    const int64_t ntail = (row_bytes - tail0) / 2;
+    [[maybe_unused]] const int64_t src_bytes = (rows - 1) * src_ld + row_bytes;
+    [[maybe_unused]] const int64_t dst_bytes = rows * dst_ld;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+#pragma unroll 4
+    for (int64_t u = first; u < rows * nvec; u += step) {
+        const int64_t r = u / nvec, c = u - r * nvec;
+        const V* sp = reinterpret_cast<const V*>(src + r * src_ld) + c;
+        V* dp = reinterpret_cast<V*>(dst + r * dst_ld) + c;
+        if (GEMM_DBG_OK(sp, src, src_bytes, sizeof(V)) && GEMM_DBG_OK(dp, dst, dst_bytes, sizeof(V)))
+            *dp = *sp;
+    }
+    if (ntail == 0) return;
+    for (int64_t u = first; u < rows * ntail; u += step) {
+        const int64_t r = u / ntail, b = tail0 + 2 * (u - r * ntail);
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(src + r * src_ld + b);
+        uint16_t* dp = reinterpret_cast<uint16_t*>(dst + r * dst_ld + b);
+        if (GEMM_DBG_OK(sp, src, src_bytes, 2) && GEMM_DBG_OK(dp, dst, dst_bytes, 2)) *dp = *sp;
     }
 }
 
@@ -259,17 +277,27 @@ __global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
 cudaError_t launch_restride(const void* src, void* dst, int64_t rows, int64_t cols,
                             int64_t src_ld, int64_t dst_ld, int es, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (es != 2 && es != 4) return cudaErrorInvalidValue;
+    const int64_t row_bytes = cols * es, sld = src_ld * es, dld = dst_ld * es;
+    const uint64_t align = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                           (uint64_t)sld | (uint64_t)dld;
+    const int v = (align & 15u) == 0 ? 16 : (align & 7u) == 0 ? 8 : (align & 3u) == 0 ? 4 : 2;
+    // up to 16 blocks of 256 threads an SM, each thread a few units
     const int threads = 256;
-    int64_t bx = (cols + threads - 1) / threads;
-    dim3 grid((unsigned)(bx < 64 ? bx : 64), (unsigned)(rows < 65535 ? rows : 65535));
-    if (es == 4)
-        restride_kernel<uint32_t><<<grid, threads, 0, stream>>>(
-            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, src_ld, dst_ld);
-    else if (es == 2)
-        restride_kernel<uint16_t><<<grid, threads, 0, stream>>>(
-            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, src_ld, dst_ld);
+    const int64_t units = rows * (row_bytes / v) + rows * ((row_bytes % v) / 2);
+    int64_t blocks = (units + threads - 1) / threads;
+    blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
+    const dim3 grid((unsigned)blocks);
+    const uint8_t* s = static_cast<const uint8_t*>(src);
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    if (v == 16)
+        restride_kernel<uint4><<<grid, threads, 0, stream>>>(s, d, rows, row_bytes, sld, dld);
+    else if (v == 8)
+        restride_kernel<uint2><<<grid, threads, 0, stream>>>(s, d, rows, row_bytes, sld, dld);
+    else if (v == 4)
+        restride_kernel<uint32_t><<<grid, threads, 0, stream>>>(s, d, rows, row_bytes, sld, dld);
     else
-        return cudaErrorInvalidValue;
+        restride_kernel<uint16_t><<<grid, threads, 0, stream>>>(s, d, rows, row_bytes, sld, dld);
     return cudaGetLastError();
 }
 
