@@ -603,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 const int col0 = n0 + c * 32;
-                if (!to_ws) epilogue_row32(epi, v, crow, C, row, col0, M, N, c_mode != kStoreScalar);
+                if (!to_ws && mode_u != kStoreScalar)
+                    epilogue_row32(epi, v, crow, C, row, col0, M, N, true);
                 if (mode_u == kStoreTma) {
                     // Stage the warp's 32 x 32 block (row = lane) with the 128-byte
                     // swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)), then
@@ -628,6 +629,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++stored;
                     }
                     stored = __shfl_sync(0xffffffffu, stored, 0);
+                } else if (mode_u == kStoreScalar) {
+                    // C rows not 16-byte aligned: stage the block (row = lane) as
+                    // above, then write it a row at a time, lane j to column
+                    // col0 + j, so that each store (and the epilogue's read of C)
+                    // covers 128 contiguous bytes instead of 32 rows.
+                    const uint32_t stg = sC + (uint32_t)(quarter * 2 * 4096);
+                    if (lane == 0) bulk_wait_group_read<0>();   // no TMA store still reads it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), v[4 * j],
+                                     v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    __syncwarp();
+                    const int col = col0 + lane;
+#pragma unroll 4
+                    for (int i = 0; i < 32; ++i) {
+                        const int r = row0 + i;
+                        if (r >= M) break;   // the same for the whole warp
+                        const float x = ld_shared_f32(
+                            stg + (uint32_t)(i * 128 + ((((lane >> 2) ^ (i & 7))) << 4) + (lane & 3) * 4));
+                        float* dst = C + (int64_t)r * N + col;
+                        if (col < N && GEMM_DBG_OK(dst, C, (int64_t)M * N * 4, 4))
+                            *dst = epilogue_apply(epi, x, dst);
+                    }
+                    __syncwarp();   // the block is read before the next chunk overwrites it
                 } else if (row < M) {
                     if (mode_u == kStoreVec && col0 + 32 <= N) {
 #pragma unroll
