@@ -98,7 +98,9 @@ struct SlabLoader {
     const float* a_ptr;                // &A[m0 + tid/8][tid % 8]
     const float* b_ptr;                // &B[tid / kBPerRow][n0 + column of this thread]
     int64_t a_group_step;              // kRowsPerPass * K: to the next row group of A
-    int64_t n;                         // N, the row stride of B
+    int64_t n;                         // the row stride of B (ldb >= N; with the
+                                       // vector copies, a chunk that crosses N reads
+                                       // the row's padding up to ldb)
     uint32_t a_row_ok;                 // bit j: row group j of this thread is < M
     bool b_col_ok;
     int a_k, b_k;                      // this thread's k offset within a slab (A, B)
@@ -109,7 +111,7 @@ struct SlabLoader {
 #endif
 
     __device__ __forceinline__ SlabLoader(const float* A, const float* B, float* sA, float* sB,
-                                          int M, int N, int K, int m0, int n0, int tid) {
+                                          int M, int N, int K, int ldb, int m0, int n0, int tid) {
         const int ar = tid >> 3;
         a_k = tid & 7;
         a_base = A;
@@ -123,12 +125,12 @@ struct SlabLoader {
         b_k = tid / kBPerRow;
         const int bc = (tid % kBPerRow) * kBElems;
         b_col_ok = n0 + bc < N;   // vec: N % 4 == 0, so the whole chunk is in or out
-        b_ptr = b_col_ok ? B + (int64_t)b_k * N + n0 + bc : B;
-        n = N;
+        b_ptr = b_col_ok ? B + (int64_t)b_k * ldb + n0 + bc : B;
+        n = ldb;
         b_dst = smem_u32(sB + b_k * kLdB + bc);
 #ifdef GEMM_DEBUG
         dbg_a = A, dbg_b = B;
-        dbg_a_bytes = (int64_t)M * K * 4, dbg_b_bytes = (int64_t)K * N * 4;
+        dbg_a_bytes = (int64_t)M * K * 4, dbg_b_bytes = (int64_t)K * ldb * 4;
 #endif
     }
 
@@ -202,7 +204,7 @@ struct SlabLoader {
 template <class CF, bool kBVec, bool kCVec, bool kWide>
 __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     ffma_sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                      float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
+                      float* __restrict__ C, int M, int N, int K, int ldb, int tiles_m, int tiles_n,
                       int dp_tiles, int splits, float* __restrict__ partial,
                       unsigned* __restrict__ counters, const Epilogue epi) {
     constexpr int TM = CF::TM, TN = CF::TN, kStages = CF::kStages;
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
         for (int j = 0; j < TN; ++j) acc2[p][j] = make_float2(0.0f, 0.0f);
     auto acc = [&](int i, int j) -> float& { return (i & 1) ? acc2[i >> 1][j].y : acc2[i >> 1][j].x; };
 
-    const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, m0, n0, tid);
+    const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, kBVec ? ldb : N, m0, n0, tid);
     const int full_slabs = K / kBK;   // slabs kt < full_slabs lie wholly inside K
     const int nloc = kt_end - kt_begin;
     // Slabs before interior_end can take the unchecked copies.
@@ -424,7 +426,7 @@ constexpr int kMaxPieces = 3;
 template <class CF, bool kBVec, bool kCVec>
 __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
     ffma_stream_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                       float* __restrict__ C, int M, int N, int K, int tiles_m, int tiles_n,
+                       float* __restrict__ C, int M, int N, int K, int ldb, int tiles_m, int tiles_n,
                        float* __restrict__ ws, unsigned* __restrict__ counters,
                        const Epilogue epi) {
     constexpr int TM = CF::TM, TN = CF::TN, kStages = CF::kStages;
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
             return (i & 1) ? acc2[i >> 1][j].y : acc2[i >> 1][j].x;
         };
 
-        const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, m0, n0, tid);
+        const SlabLoader<kBVec, CF::kThreads> loader(A, B, sA, sB, M, N, K, kBVec ? ldb : N, m0, n0, tid);
         const int nloc = kt_end - kt_begin;
         const bool interior = m0 + kBM <= M && n0 + kBN <= N;
         const int interior_end = interior ? full_slabs : 0;
@@ -764,21 +766,22 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
 // without it.
 template <bool BV, bool CV>
 static void launch_variant(dim3 grid, size_t smem, cudaStream_t stream, const float* A,
-                           const float* B, float* C, int M, int N, int K, int tiles_m,
+                           const float* B, float* C, int M, int N, int K, int ldb, int tiles_m,
                            int tiles_n, int dp, int sp, const FfmaPlan& plan, float* partial,
                            unsigned* counters, float* ws, const Epilogue& epi) {
     if (plan.wide)
         ffma_sgemm_kernel<FfmaCfg, BV, CV, true><<<grid, FfmaCfg::kThreads, smem, stream>>>(
-            A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, ws, nullptr, kPlainStore);
+            A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp, sp, ws, nullptr, kPlainStore);
     else
         ffma_sgemm_kernel<FfmaCfg, BV, CV, false><<<grid, FfmaCfg::kThreads, smem, stream>>>(
-            A, B, C, M, N, K, tiles_m, tiles_n, dp, sp, partial, counters, epi);
+            A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp, sp, partial, counters, epi);
 }
 
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
-                              bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, const Epilogue& epi, float* ws,
+                              int ldb, bool b_vec, bool c_vec, const FfmaPlan& plan,
+                              float* partial, unsigned* counters, const Epilogue& epi, float* ws,
                               cudaStream_t stream) {
+    if (ldb < N || (b_vec && ldb % 4 != 0)) return cudaErrorInvalidValue;
     const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     if (plan.tiles <= 0) return cudaSuccess;
     if (plan.stream) {
@@ -799,17 +802,17 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
         cfg.numAttrs = kUsePdl ? 1 : 0;
         cudaError_t e;
         if (b_vec && c_vec)
-            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, true>, A, B, C, M, N, K,
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, true>, A, B, C, M, N, K, ldb,
                                    tiles_m, tiles_n, ws, counters, epi);
         else if (b_vec)
-            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, false>, A, B, C, M, N, K,
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, true, false>, A, B, C, M, N, K, ldb,
                                    tiles_m, tiles_n, ws, counters, epi);
         else if (c_vec)
-            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, false, true>, A, B, C, M, N, K,
+            e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, false, true>, A, B, C, M, N, K, ldb,
                                    tiles_m, tiles_n, ws, counters, epi);
         else
             e = cudaLaunchKernelEx(&cfg, ffma_stream_kernel<FfmaCfg, false, false>, A, B, C, M, N,
-                                   K, tiles_m, tiles_n, ws, counters, epi);
+                                   K, ldb, tiles_m, tiles_n, ws, counters, epi);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     const int64_t ctas = plan.dp_tiles + plan.split_tiles * plan.splits;
@@ -818,16 +821,16 @@ cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, i
     const int dp = (int)plan.dp_tiles, sp = plan.splits;
     const size_t smem = FfmaCfg::kSmemBytes;
     if (b_vec && c_vec)
-        launch_variant<true, true>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+        launch_variant<true, true>(grid, smem, stream, A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp, sp,
                                    plan, partial, counters, ws, epi);
     else if (b_vec)
-        launch_variant<true, false>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+        launch_variant<true, false>(grid, smem, stream, A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp, sp,
                                     plan, partial, counters, ws, epi);
     else if (c_vec)
-        launch_variant<false, true>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp, sp,
+        launch_variant<false, true>(grid, smem, stream, A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp, sp,
                                     plan, partial, counters, ws, epi);
     else
-        launch_variant<false, false>(grid, smem, stream, A, B, C, M, N, K, tiles_m, tiles_n, dp,
+        launch_variant<false, false>(grid, smem, stream, A, B, C, M, N, K, ldb, tiles_m, tiles_n, dp,
                                      sp, plan, partial, counters, ws, epi);
     return cudaGetLastError();
 }

@@ -70,8 +70,8 @@ struct FfmaPlan {
 cudaError_t ffma_setup();
 FfmaPlan ffma_plan(int M, int N, int K, int num_sms);
 cudaError_t launch_ffma_sgemm(const float* A, const float* B, float* C, int M, int N, int K,
-                              bool b_vec, bool c_vec, const FfmaPlan& plan, float* partial,
-                              unsigned* counters, const Epilogue& epi, float* ws,
+                              int ldb, bool b_vec, bool c_vec, const FfmaPlan& plan,
+                              float* partial, unsigned* counters, const Epilogue& epi, float* ws,
                               cudaStream_t stream);
 
 

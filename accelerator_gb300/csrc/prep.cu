@@ -23,9 +23,10 @@ namespace {
 // Rows of row_bytes bytes from stride src_ld to stride dst_ld (both in
 // bytes), copied V bytes at a time -- V the widest unit that divides both
 // bases and both strides -- and the rows' last row_bytes % V bytes two at a
-// time (elements are 2 or 4 bytes).  One flat index runs over all (row,
-// unit) pairs, so consecutive threads copy consecutive units and every
-// thread has several independent copies in flight.
+// time (elements are 2 or 4 bytes); the padding after each destination row
+// is zeroed.  One flat index runs over all (row, unit) pairs, so
+// consecutive threads copy consecutive units and every thread has several
+// independent copies in flight.
 template <typename V>
 __global__ void restride_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                 int64_t rows, int64_t row_bytes, int64_t src_ld, int64_t dst_ld) {
@@ -43,12 +44,19 @@ __global__ void restride_kernel(const uint8_t* __restrict__ src, uint8_t* __rest
         if (GEMM_DBG_OK(sp, src, src_bytes, sizeof(V)) && GEMM_DBG_OK(dp, dst, dst_bytes, sizeof(V)))
             *dp = *sp;
     }
-    if (ntail == 0) return;
     for (int64_t u = first; u < rows * ntail; u += step) {
         const int64_t r = u / ntail, b = tail0 + 2 * (u - r * ntail);
         const uint16_t* sp = reinterpret_cast<const uint16_t*>(src + r * src_ld + b);
         uint16_t* dp = reinterpret_cast<uint16_t*>(dst + r * dst_ld + b);
         if (GEMM_DBG_OK(sp, src, src_bytes, 2) && GEMM_DBG_OK(dp, dst, dst_bytes, 2)) *dp = *sp;
+    }
+    // each destination row's padding (row_bytes .. dst_ld) is zeroed: a
+    // reader may load it with the row's last vector
+    const int64_t npad = (dst_ld - row_bytes) / 2;
+    for (int64_t u = first; u < rows * npad; u += step) {
+        const int64_t r = u / npad, b = row_bytes + 2 * (u - r * npad);
+        uint16_t* dp = reinterpret_cast<uint16_t*>(dst + r * dst_ld + b);
+        if (GEMM_DBG_OK(dp, dst, dst_bytes, 2)) *dp = 0;
     }
 }
 
