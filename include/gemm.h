@@ -121,7 +121,10 @@ enum gemm_status {
  * meets a row stride that is not a multiple of 16 bytes, or a base address
  * that is not 16-byte aligned, the operand is first copied into a scratch
  * buffer with a padded row stride; that buffer is taken from and returned to
- * CUDA's stream-ordered allocator on `stream` inside the call.
+ * CUDA's stream-ordered allocator on `stream` inside the call.  GEMM_FP32
+ * does the same for B (K * roundup(N, 4) floats) when B's rows are not
+ * 16-byte aligned and M >= 1024, so that B can be read 16 bytes at a time;
+ * the K-split forms of both paths take workspace from the same allocator.
  * Returns GEMM_OK or an enum gemm_status code; on an error nothing is enqueued.
  */
 GEMM_API int gemm(const void* A, const void* B, float* C, int64_t M, int64_t K, int64_t N,
