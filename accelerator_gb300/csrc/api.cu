@@ -322,7 +322,9 @@ int tensor_core_gemm(TcMode mode, const void* A, const void* B, float* C, int64_
 // (with the split workspace, when the product is split, after them).
 int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
                       const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
-    const int64_t lda = round_up(K, 8), ldb = round_up(N, 8);
+    // A's rows in whole 128-byte lines (no box row straddles two); B's in
+    // 16-byte chunks, so that B stays in the atom-ordered form when N allows
+    const int64_t lda = round_up(K, 64), ldb = round_up(N, 8);
     const int64_t a_bytes = round_up(M * lda * 2, 256), b_bytes = round_up(K * ldb * 2, 256);
     const TcSplit split = tc_plan_split(TcMode::kBF16, M, N, K);
     const int64_t ws_bytes = round_up(tc_split_workspace_bytes(split, M, N), 256);
@@ -351,7 +353,8 @@ int rounded_bf16_gemm(const float* A, const float* B, float* C, int64_t M, int64
 // product is split, after them).
 int rounded_tf32_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, int64_t N,
                       const Epilogue& epi, DeviceState* st, cudaStream_t stream) {
-    const int64_t lda = round_up(K, 4), ldb = round_up(N, 4);
+    // A's rows in whole 128-byte lines, B's in 16-byte chunks (as above)
+    const int64_t lda = round_up(K, 32), ldb = round_up(N, 4);
     const int64_t a_bytes = round_up(M * lda * 4, 256), b_bytes = round_up(K * ldb * 4, 256);
     const TcSplit split = tc_plan_split(TcMode::kTF32, M, N, K);
     const int64_t ws_bytes = round_up(tc_split_workspace_bytes(split, M, N), 256);
@@ -401,7 +404,9 @@ TcPlan tc_plan(TcMode mode, const void* A, const void* B, int64_t M, int64_t K, 
     // B is read as the caller stores it (K x N rows, MN-major) in every mode.
     p.pad_a = (K % align_elems) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
     p.pad_b = (N % align_elems) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
-    p.lda = p.pad_a ? round_up(K, align_elems) : K;
+    // a re-strided A gets rows of whole 128-byte lines, so that no row of an
+    // A box straddles two lines
+    p.lda = p.pad_a ? round_up(K, 128 / es) : K;
     p.ldb = p.pad_b ? round_up(N, align_elems) : N;
     p.a_bytes = p.pad_a ? round_up(M * p.lda * es, 256) : 0;
     p.b_bytes = p.pad_b ? round_up(K * p.ldb * es, 256) : 0;
