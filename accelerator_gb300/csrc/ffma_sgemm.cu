@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
 // the CTA that stores a tile's last piece (in time) adds all of its pieces
 // in K order and stores C: C_ij is then ((p0 + p1) + p2), the same on every
 // run.  With at least half a wave of tiles a CTA's range is longer than
-// half a tile, so a tile has at most three pieces (kMaxPieces).
+// half a tile, so a tile has at most three pieces (kMaxPieces); with a
+// quarter to half a wave it can have up to five, and the pieces past the
+// third are added one by one after them, still in K order.
 
 // Tile coordinates in the grouped raster (kGroupM tile-rows per group).
 __device__ __forceinline__ void ffma_tile_coords(int tile, int tiles_m, int tiles_n, int& m0,
@@ -588,8 +590,8 @@ __global__ void __launch_bounds__(CF::kThreads, CF::kMinBlocks)
                                      (int64_t)(kBM * kBN);
                 }
                 // eight fragments at a time, every piece's loads issued before the
-                // adds (pieces beyond kMaxPieces, which the planner's range rules
-                // out, are added one by one after them, still in K order)
+                // adds (pieces beyond kMaxPieces, which only ranges shorter than
+                // half a tile make, are added one by one after them, in K order)
 #pragma unroll
                 for (int f0 = 0; f0 < TM * (TN / 4); f0 += 8) {
                     float4 v[kMaxPieces][8];
@@ -693,13 +695,31 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
     // kept for the split tiles of a last wave, is latency-bound: 2 splits of
     // a 256^3 product took 53 us in the kernel against 24 us this way.)
     constexpr int64_t kMinSlabsWide = 4, kMaxWorkspace = 512ll << 20;
+    // Stream-K (below): one persistent CTA per slot, between a quarter of a
+    // wave and two waves of tiles, with K long enough that a CTA's range
+    // holds at least kMinStreamSlabs slabs (GEMM_FORCE_CONFIG=ffma_no_stream
+    // disables it).
+    constexpr int64_t kMinStreamSlabs = 32, kStreamCost = 8, kSplitCost = 8, kMinSlabs = 8;
+    static const bool no_stream = [] {
+        const char* f = std::getenv("GEMM_FORCE_CONFIG");
+        return f && std::strcmp(f, "ffma_no_stream") == 0;
+    }();
+    const int64_t total = tiles * nkt;
+    bool stream_k = !no_stream && slots > 0 && 4 * tiles > slots && tiles < 2 * slots &&
+                    tiles % slots != 0 && total >= kMinStreamSlabs * slots;
     if (slots > 0 && tiles < slots && slots / tiles >= 2 && nkt >= 2 * kMinSlabsWide) {
         int64_t s = slots / tiles;
         if (s > nkt / kMinSlabsWide) s = nkt / kMinSlabsWide;
         if (s > 256) s = 256;
         const int64_t block = (int64_t)M * N * (int64_t)sizeof(float);
         if (s * block > kMaxWorkspace) s = kMaxWorkspace / block;
-        if (s >= 2) {
+        // Below half a wave stream-K is taken instead when the split's s x
+        // tiles CTAs would leave more than 7 % of the slots idle (889 x
+        // 4037 x 2830: 606 -> 454 us; 1500 x 3000 x 1800: 400 -> 348 us);
+        // where they fill the slots the split stays (1536 x 2048 x 1536: 186
+        // against 192 us).
+        const bool sk_instead = stream_k && s * tiles * 100 < slots * 93;
+        if (s >= 2 && !sk_instead) {
             p.splits = (int)s;
             p.dp_tiles = 0;
             p.split_tiles = tiles;
@@ -708,25 +728,14 @@ FfmaPlan ffma_plan(int M, int N, int K, int num_sms) {
             return p;
         }
     }
-    // Between half a wave and two waves of tiles, with K long enough that a
-    // CTA's range holds at least kMinStreamSlabs slabs: stream-K, one
-    // persistent CTA per slot (GEMM_FORCE_CONFIG=ffma_no_stream disables it).
-    // Under one wave it is always taken (whole tiles leave slots idle: 2048^3
-    // 365 -> 309 us, 2432^3 603 -> 498 us).  From one to two waves it is
-    // taken when its cost in slab times, an equal share plus kStreamCost
-    // (restarts and the partial tiles), is under 97 % of a full wave plus the
-    // last wave as split below (its pieces plus kSplitCost): measured 3072^3
-    // 1069 -> 977 us and 3584^3 1694 -> 1528 us taken; 2944^3 (tail split 6
-    // ways, 850 against 866 us) and 3840^3 (1.97 waves, 1815 against 1863 us)
-    // left as they were.
-    constexpr int64_t kMinStreamSlabs = 32, kStreamCost = 8, kSplitCost = 8, kMinSlabs = 8;
-    static const bool no_stream = [] {
-        const char* f = std::getenv("GEMM_FORCE_CONFIG");
-        return f && std::strcmp(f, "ffma_no_stream") == 0;
-    }();
-    const int64_t total = tiles * nkt;
-    bool stream_k = !no_stream && slots > 0 && 2 * tiles > slots && tiles < 2 * slots &&
-                    tiles % slots != 0 && total >= kMinStreamSlabs * slots;
+    // Stream-K under one wave is always taken (whole tiles leave slots
+    // idle: 2048^3 365 -> 309 us, 2432^3 603 -> 498 us).  From one to two
+    // waves it is taken when its cost in slab times, an equal share plus
+    // kStreamCost (restarts and the partial tiles), is under 97 % of a full
+    // wave plus the last wave as split below (its pieces plus kSplitCost):
+    // measured 3072^3 1069 -> 977 us and 3584^3 1694 -> 1528 us taken; 2944^3
+    // (tail split 6 ways, 850 against 866 us) and 3840^3 (1.97 waves, 1815
+    // against 1863 us) left as they were.
     if (stream_k && tiles > slots) {
         int64_t s = slots / (tiles - slots);
         if (s > nkt / kMinSlabs) s = nkt / kMinSlabs;

@@ -90,6 +90,7 @@ else:
     # by the CTA of its last piece): vector and scalar B and C
     check("fp32", 2000, 1601, 2100, sampled=True)
     check("fp32", 1990, 1601, 2102, sampled=True, alpha=0.5, beta=-1.25)
+    check("fp32", 1000, 3000, 1900, sampled=True)   # up to five pieces a tile
     # tensor kernels: re-strided A (K % 4 != 0), re-strided B and scalar
     # stores (N % 4 != 0),
     # all tiles split (one pair tile, long K), the last round split
@@ -124,7 +125,7 @@ def _child(env_extra):
 @pytest.mark.gpu
 def test_debug_build_all_paths_in_bounds():
     out = _child({})
-    assert out.count("ok ") == 33
+    assert out.count("ok ") == 34
 
 
 @pytest.mark.gpu

@@ -20,7 +20,9 @@ pytestmark = pytest.mark.gpu
 
 # (M, K, N): 256 tiles x 128 slabs; 576 tiles x 64 slabs; 272 ragged tiles
 # x 101 slabs (K = 1601: the last slab partial)
-SHAPES = [(2048, 2048, 2048), (3072, 1024, 3072), (2000, 1601, 2100)]
+# the last: a quarter to half a wave of tiles with long K, where a tile has
+# up to five pieces (those past the third added one by one)
+SHAPES = [(2048, 2048, 2048), (3072, 1024, 3072), (2000, 1601, 2100), (1000, 3000, 1900)]
 
 
 @pytest.mark.parametrize("M,K,N", SHAPES)
