@@ -404,10 +404,11 @@ TcPlan tc_plan(TcMode mode, const void* A, const void* B, int64_t M, int64_t K, 
     // B is read as the caller stores it (K x N rows, MN-major) in every mode.
     p.pad_a = (K % align_elems) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
     p.pad_b = (N % align_elems) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
-    // a re-strided A gets rows of whole 128-byte lines, so that no row of an
-    // A box straddles two lines
+    // a re-strided operand gets rows of whole 128-byte lines, so that no row
+    // of a box straddles two lines (a re-strided B is read in 2-D boxes
+    // anyway: the atom-ordered form needs ldb == N)
     p.lda = p.pad_a ? round_up(K, 128 / es) : K;
-    p.ldb = p.pad_b ? round_up(N, align_elems) : N;
+    p.ldb = p.pad_b ? round_up(N, 128 / es) : N;
     p.a_bytes = p.pad_a ? round_up(M * p.lda * es, 256) : 0;
     p.b_bytes = p.pad_b ? round_up(K * p.ldb * es, 256) : 0;
     p.split = tc_plan_split(mode, M, N, K);

@@ -216,7 +216,7 @@ GEMM_API int gemm_selftest_bounded_wait(int64_t timeout_ns, struct CUstream_st* 
  * C equals gemm()'s C bit for bit.  K == 0 gives C = 0.
  *
  * Limit: the scratch gemm() would take for the product -- 4 * M * roundup(K, 32)
- * bytes for a re-strided A, 4 * K * roundup(N, 4) for a re-strided B, and
+ * bytes for a re-strided A, 4 * K * roundup(N, 32) for a re-strided B, and
  * 256 KB per split piece of the K split, each rounded up to 256 bytes -- must
  * not exceed GEMM_NOALLOC_SCRATCH_BYTES (64 MiB).  Aligned products with
  * K, N multiples of 4 need at most the split workspace (14.7 MB at 4096^3,

@@ -118,7 +118,7 @@ def test_noalloc_k_zero_writes_zeros(libgemm):
 
 def test_noalloc_rejects_products_beyond_its_buffer(libgemm):
     import torch
-    # a re-strided B of 4096 x roundup(4097, 4) floats is just over 64 MiB
+    # a re-strided B of 4096 x roundup(4097, 32) floats is just over 64 MiB
     M, K, N = 16, 4096, 4097
     a = torch.zeros((M, K), device="cuda")
     b = torch.zeros((K, N), device="cuda")
