@@ -196,12 +196,14 @@ int ffma_gemm(const float* A, const float* B, float* C, int64_t M, int64_t K, in
         g_launches++;
         return GEMM_OK;
     }
-    if (b_vec || M < 1024) return ffma_product(A, B, N, b_vec, C, M, K, N, c_vec, epi, st, stream);
     // B rows that are not whole 16-byte chunks would be copied 4 bytes at a
-    // time by every tile; with at least 1024 rows of A to amortise it, B is
-    // re-strided once into rows padded to 16 bytes (padding zeroed) and read
-    // 16 bytes at a time.  (4096 x 4096 x 4090: 2.69 -> 2.26 ms; at M = 256
-    // the copy cost more than it saved.)
+    // time by every tile; with at least kRestrideRows rows of A to amortise
+    // it, B is re-strided once into rows padded to 16 bytes (padding zeroed)
+    // and read 16 bytes at a time.  (4096 x 4096 x 4090: 2.69 -> 2.26 ms; at
+    // M = 256 the copy cost more than it saved.)
+    constexpr int64_t kRestrideRows = 1024;
+    if (b_vec || M < kRestrideRows)
+        return ffma_product(A, B, N, b_vec, C, M, K, N, c_vec, epi, st, stream);
     const int64_t ldb = round_up(N, 4);
     void* b_scratch = nullptr;
     if (cudaMallocFromPoolAsync(&b_scratch, (size_t)round_up(K * ldb * 4, 256), st->pool,
