@@ -27,8 +27,8 @@
  * column block even where the atom-ordered 4-D form applies (same results,
  * bit for bit); =ffma_small / =ffma_tiles128 make every GEMM_FP32 product
  * take the 32 x 32-tile or the 128 x 128-tile FFMA kernel instead of the one
- * chosen by shape; =ffma_no_stream keeps GEMM_FP32 products of half a wave to
- * two waves of tiles off the stream-K form.  Results stay within each mode's
+ * chosen by shape; =ffma_no_stream keeps GEMM_FP32 products of a quarter of a
+ * wave to two waves of tiles off the stream-K form.  Results stay within each mode's
  * tolerance.
  */
 #ifndef LIBGEMM_GEMM_H
